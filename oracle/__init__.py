@@ -1,0 +1,14 @@
+"""CPU oracle for the Ulysses QKV front end (test infrastructure).
+
+A plain, slow, float64 restatement of what the method computes, written from
+the pages' definitions.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import it.  The product path (the CUDA library and its
+binding) never imports, calls or links anything here, and the two share no
+code: the only common module is the seeded input generator, which holds none
+of the method's arithmetic.
+
+Every function is pinned by `tests/test_oracle_pins.py` to facts fixed outside
+the oracle itself (closed forms, invariants, brute force on tiny inputs and the
+hand-written fixtures under `tests/golden/`).  No function is "parity unpinned".
+"""
+from .qnre_oracle import *  # noqa: F401,F403
