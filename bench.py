@@ -1,0 +1,408 @@
+"""Benchmark of the Ulysses QKV front end on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one batch of the workload
+"h4096_p4_s4096" (P=4 virtual ranks x B=1 x S_local=1024 tokens, hidden 4096,
+32 heads, bshd):
+  1. qnre_forward: fused QKV projection + RMSNorm + RoPE + band scatter of all
+     4096 tokens into the 4 ranks' [B, S_global, 8, 128] bands;
+  2. ulysses_pack_head_chunk for each band of the uneven schedule
+     [(0,2),(2,4),(6,2)] over H_local = 8, on strided q/k/v views of a
+     [P*B, S_local, 3, 32, 128] projection buffer (all virtual ranks in one call);
+  3. ulysses_merge_output_head_chunk of each packed band's q slice back into a
+     [P*B, S_local, 32, 128] output (pack then merge reproduces q).
+The L2 (129 MB) is flushed with a 512 MB write between timed steps.
+
+value = tokens per second of the whole step (all ranks' tokens / step time).
+
+`--impl reference` times the CPU oracle on the host cores instead: every step
+is a bounded sample of the same workload (a stratified token subset through the
+fp64 projection/norm/RoPE/placement and the same rows through pack/merge).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from ulysses_qkv_proj_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "fused QKV+norm+RoPE+scatter tokens/s & % bf16 TC peak; pack/merge GB/s % HBM"
+WORKLOAD = WL.FUSED_WORKLOADS[WL.BENCH_FUSED]
+SCHEDULE = WL.BENCH_SCHEDULE
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ----------------------------------------------------------------------------
+# clocks sampling during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from ulysses_qkv_proj_gb300 import binding as qb
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = WORKLOAD
+    peaks, peak_src = load_peaks()
+
+    def t16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    inp = WL.make_fused_inputs(wl)
+    x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x = x_host.to(dev)
+    w = t16(inp.w)
+    qw, kw = t16(inp.q_norm_w), t16(inp.k_norm_w)
+    cs = torch.from_numpy(inp.cos_sin).to(dev)
+    pos = torch.from_numpy(inp.positions).to(dev)
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
+    out = qb.alloc_outputs(plan, wl.B, wl.S, dev)
+
+    # head-chunk inputs: q/k/v views of a [P*B, S, 3, H, D] projection buffer
+    PB, S, H, D, W, L = wl.P * wl.B, wl.S, wl.num_heads, 128, wl.P, wl.H_local
+    qkv_host_np = WL.make_headchunk_buffer(PB, S, H, D)
+    qkv_host = torch.from_numpy(qkv_host_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qkv = qkv_host.to(dev)
+    packed = [torch.empty((PB, S, W * cnt, 3 * D), dtype=torch.bfloat16, device=dev) for _, cnt in SCHEDULE]
+    merged = torch.empty((PB, S, H, D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x_in, qkv_in, ev=None):
+        if ev:
+            ev[0].record()
+        qb.qnre_forward(plan, x_in, w, qw, kw, cs, pos, out)
+        if ev:
+            ev[1].record()
+        q, k, v = qkv_in[:, :, 0], qkv_in[:, :, 1], qkv_in[:, :, 2]
+        for i, (off, cnt) in enumerate(SCHEDULE):
+            qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, packed[i])
+        if ev:
+            ev[2].record()
+        for i, (off, cnt) in enumerate(SCHEDULE):
+            qb.ulysses_merge_output_head_chunk(packed[i][..., :D], W, L, off, merged)
+        if ev:
+            ev[3].record()
+
+    launches_per_step = 1 + 2 * len(SCHEDULE)
+    for _ in range(args.warmup):
+        step(x, qkv)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if plan.device_status() != 0:
+        raise RuntimeError("device status raised during warm-up")
+    if not torch.equal(merged, qkv[:, :, 0]):
+        raise RuntimeError("pack -> merge did not reproduce q")
+
+    # ---- device-resident timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(x, qkv, evs[i])
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    fused_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    pack_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = wl.T
+    value = tokens_per_step * world / (ms_per_step * 1e-3)
+
+    # ---- end to end: pinned host inputs in, results back to pinned host memory
+    out_host = {g: torch.empty_like(t, device="cpu").pin_memory() for g, t in out.items()}
+    merged_host = torch.empty_like(merged, device="cpu").pin_memory()
+    h2d = x_host.numel() * 2 + qkv_host.numel() * 2
+    d2h = sum(t.numel() * 2 for t in out.values()) + merged.numel() * 2
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    x_dev2 = torch.empty_like(x)
+    qkv_dev2 = torch.empty_like(qkv)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e2e_ev[i][0].record()
+        x_dev2.copy_(x_host, non_blocking=True)
+        qkv_dev2.copy_(qkv_host, non_blocking=True)
+        step(x_dev2, qkv_dev2)
+        for g, t in out.items():
+            out_host[g].copy_(t, non_blocking=True)
+        merged_host.copy_(merged, non_blocking=True)
+        e2e_ev[i][1].record()
+        torch.cuda.synchronize()
+        flush.zero_()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = tokens_per_step * world / (e2e_ms * 1e-3)
+
+    # ---- rooflines
+    flops = wl.flops()
+    fused_avg = statistics.mean(fused_ms)
+    tflops = flops / (fused_avg * 1e-3) / 1e12
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    elt = 2
+    pack_bytes = sum(2 * PB * S * W * cnt * 3 * D * elt for _, cnt in SCHEDULE)
+    merge_bytes = sum(2 * PB * S * W * cnt * D * elt for _, cnt in SCHEDULE)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    pack_gbs = pack_bytes / (statistics.mean(pack_ms) * 1e-3) / 1e9
+    merge_gbs = merge_bytes / (statistics.mean(merge_ms) * 1e-3) / 1e9
+
+    if rank == 0:
+        cpu = cpu_baseline(args.cpu_sample_tokens) if world == 1 else None
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/hidden) weights)",
+            "config": {"workload": f"{wl.name}: P={wl.P} B={wl.B} S_local={wl.S} hidden={wl.hidden} "
+                                   f"heads={wl.num_heads} layout={wl.layout} rope={wl.rope_style}; "
+                                   f"pack/merge schedule {list(SCHEDULE)} over H_local={L}",
+                       "tokens_per_step": tokens_per_step, "P": wl.P, "B": wl.B, "S_local": wl.S,
+                       "hidden": wl.hidden, "num_heads": wl.num_heads, "layout": wl.layout,
+                       "schedule": [list(b) for b in SCHEDULE], "l2": "flushed (512 MB write) between steps",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": round(tflops / tc_peak, 4), "traffic": None,
+                         "kernel": "fused_qkv_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "flops_per_launch": flops},
+            "fused": {"ms": round(fused_avg, 5), "tflops": round(tflops, 1), "tokens_per_s": round(wl.T / (fused_avg * 1e-3), 1)},
+            "pack": {"ms": round(statistics.mean(pack_ms), 5), "bytes": pack_bytes, "GB/s": round(pack_gbs, 1),
+                     "frac_hbm": round(pack_gbs / hbm_peak, 4), "launches": len(SCHEDULE)},
+            "merge": {"ms": round(statistics.mean(merge_ms), 5), "bytes": merge_bytes, "GB/s": round(merge_gbs, 1),
+                      "frac_hbm": round(merge_gbs / hbm_peak, 4), "launches": len(SCHEDULE)},
+            "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "wall_s_timed": round(t_wall, 4),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+_CPU_CACHE = {}
+
+
+def _cpu_inputs():
+    if "inp" not in _CPU_CACHE:
+        wl = WORKLOAD
+        _CPU_CACHE["inp"] = WL.make_fused_inputs(wl)
+        _CPU_CACHE["qkv"] = WL.make_headchunk_buffer(wl.P * wl.B, wl.S, wl.num_heads, 128)
+    return _CPU_CACHE["inp"], _CPU_CACHE["qkv"]
+
+
+def cpu_sample_step(n_tokens: int):
+    """One step of the workload on the CPU oracle, on n_tokens of its tokens; returns (tokens, seconds).
+
+    n_tokens >= T runs the whole workload (oracle.qnre_forward + pack/merge of every row);
+    fewer tokens take a stratified random subset (projection/norm/RoPE of those tokens,
+    their band destinations, and pack/merge of the same number of rows).
+    """
+    import oracle
+    wl = WORKLOAD
+    inp, qkv = _cpu_inputs()
+    t0 = time.perf_counter()
+    if n_tokens >= wl.T:
+        n_tokens = wl.T
+        res = oracle.qnre_forward(inp.x, inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin, inp.positions,
+                                  wl.P, wl.num_heads, wl.layout, wl.rope_style)
+        assert all(not np.isnan(a).any() for a in res.values())
+        rows = wl.S
+    else:
+        rng = np.random.default_rng(123)
+        tok = np.sort(rng.choice(wl.T, size=n_tokens, replace=False))
+        x2 = inp.x.reshape(wl.T, wl.hidden)
+        O = oracle.project_norm_rope(x2[tok], inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin,
+                                     inp.positions.reshape(-1)[tok], wl.num_heads, wl.rope_style)
+        dest = [oracle.band_destination(*oracle.token_coords(int(t), wl.P, wl.B, wl.S), h, wl.P, wl.B, wl.S,
+                                        wl.num_heads) for t in tok for h in range(wl.num_heads)]
+        assert O.shape[0] == n_tokens and len(dest) == n_tokens * wl.num_heads
+        rows = max(1, n_tokens // (wl.P * wl.B))
+    sub = qkv[:, :rows]
+    merged = np.zeros((wl.P * wl.B, rows, wl.num_heads, 128), np.uint16)
+    for off, cnt in SCHEDULE:
+        pk = oracle.pack_head_chunk(sub[:, :, 0], sub[:, :, 1], sub[:, :, 2], wl.P, off, cnt)
+        merged = oracle.merge_output_head_chunk(pk[..., :128], wl.P, wl.H_local, off, merged)
+    dt = time.perf_counter() - t0
+    return n_tokens, dt
+
+
+def cpu_cores() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(n_tokens: int):
+    cpu_sample_step(32)  # warm the input cache and BLAS
+    tok, dt = cpu_sample_step(n_tokens)
+    what = ("the whole workload" if tok >= WORKLOAD.T else f"{tok} of {WORKLOAD.T} tokens (stratified random)")
+    return {"value": round(tok / dt, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{what} of {WORKLOAD.name} through the fp64 oracle (projection, RMSNorm, RoPE, band "
+                      f"placement) plus pack+merge of the matching rows over the same schedule; numpy BLAS "
+                      f"threads = cores",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    _cpu_inputs()
+    # size each step so that warm-up + timed steps take about 90 s of CPU time
+    n_cal, dt_cal = cpu_sample_step(64)
+    per_token = dt_cal / n_cal
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(WORKLOAD.T, budget / per_token)))
+    for _ in range(args.warmup):
+        cpu_sample_step(n)
+    times = []
+    for _ in range(args.steps):
+        tok, dt = cpu_sample_step(n)
+        times.append(dt)
+    ms_per_step = 1e3 * sum(times) / len(times)
+    value = tok / (ms_per_step * 1e-3)
+    wl = WORKLOAD
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "tokens_per_step_sample": tok,
+                                        "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{tok} of {wl.T} tokens per step (stratified random) through the fp64 "
+                                   f"oracle, plus pack+merge of the matching rows"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

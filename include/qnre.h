@@ -1,0 +1,229 @@
+/*
+ * qnre.h -- C ABI of libqnre: the single-GPU data-parallel core of the Ulysses
+ * sequence-parallel attention front end, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (pages, by title and section):
+ *   [FUSED] flashinfer.comm API reference v0.7.4, "Fused QKV Projection + Norm +
+ *           RoPE + Head Exchange" (QkvNormRopeExchangeOverlap and its Notes).
+ *   [MATH]  "QKV projection + RMSNorm + RoPE overlapped with the Ulysses head
+ *           exchange" (flashinfer PR #6332 commit text, on the docs PR #4240
+ *           page), "Description" and "Assumptions" / "Operator math".
+ *   [ULY]   flashinfer.comm API reference, "Ulysses Context-Parallel All-to-All".
+ *   [PACK]  flashinfer.comm API reference, "Head-Chunk Layout and Transport
+ *           Primitives", pack_ulysses_qkv_head_chunk.
+ *   [MERGE] same section, merge_ulysses_output_head_chunk.
+ *   [PR5027] "allocation-stable, head-chunked Ulysses communication primitives"
+ *           (flashinfer PR #5027), Description: uneven schedules, positive-stride
+ *           non-contiguous views, storage-range alias checks, int32 limits.
+ *
+ * On one GPU the P Ulysses ranks are virtual: every rank's input shard and
+ * every rank's receive buffer live in this GPU's memory, and the head exchange
+ * is the address each result is stored to.  No call communicates.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" point to memory of the current CUDA device; the
+ *     caller owns all of it.  No call allocates device memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without waiting for it.
+ *   - Arguments are validated before anything is launched: a call that returns
+ *     an error has enqueued nothing and written nothing.
+ *   - bf16 values are IEEE bfloat16 bit patterns (the high half of a float32).
+ *   - Status codes: QNRE_OK on success, else the first failed check.
+ */
+#ifndef QNRE_H_
+#define QNRE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QNRE_HEAD_DIM 128
+
+typedef struct CUstream_st* qnre_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  QNRE_OK = 0,
+  QNRE_ERR_INVALID_ARG = 1, /* bad shape, count, offset, NULL pointer, unknown enum */
+  QNRE_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (head_dim != 128, dtype) */
+  QNRE_ERR_ALIGNMENT = 3,   /* a pointer or stride breaks the stated byte alignment */
+  QNRE_ERR_ALIAS = 4,       /* an output's storage range overlaps an input's */
+  QNRE_ERR_CAPACITY = 5,    /* B*S_local > max_tokens, or a size that overflows 64-bit offsets */
+  QNRE_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed (no device, launch failure) */
+  QNRE_ERR_DEVICE = 7       /* a device-side check fired (see qnre_plan_device_status) */
+} qnre_status_t;
+
+typedef enum { QNRE_LAYOUT_BSHD = 0, QNRE_LAYOUT_FUSED = 1 } qnre_layout_t;
+
+/* RoPE pairing.  ROTATE_HALF rotates (i, i+64); INTERLEAVED rotates (2i, 2i+1)
+ * (the pairing the [MATH] page names).  Both read cos_i = cos_sin[p][i] and
+ * sin_i = cos_sin[p][64+i], i < 64. */
+typedef enum { QNRE_ROPE_ROTATE_HALF = 0, QNRE_ROPE_INTERLEAVED = 1 } qnre_rope_t;
+
+typedef enum { QNRE_DTYPE_BF16 = 0, QNRE_DTYPE_FP16 = 1, QNRE_DTYPE_FP32 = 2 } qnre_dtype_t;
+
+/* Plan flags. */
+#define QNRE_FLAG_EPILOGUE_OFF 0x1u /* store the bare projection for q, k and v (no norm, no RoPE).
+                                       A diagnostic: with integer-coded inputs the result is exact,
+                                       so band placement can be compared bit for bit. */
+
+/* Device-side status bits (qnre_plan_device_status). */
+#define QNRE_DEVICE_BAD_POSITION 0x1u /* a token's position was outside [0, n_pos): its q and k rows
+                                         were written as NaN and the table was not read */
+#define QNRE_DEVICE_WAIT_TIMEOUT 0x2u /* a pipeline wait inside the kernel ran past its time limit; the
+                                         kernel stopped early and its outputs are incomplete */
+
+typedef struct qnre_plan_s* qnre_plan_t;
+
+/* Output buffers of qnre_forward (device, bf16, caller-owned, 16-byte aligned).
+ *   QNRE_LAYOUT_BSHD : q, k, v each [P, B, S_global, H_local, 128]; fused unused.
+ *   QNRE_LAYOUT_FUSED: fused [P, B, S_global, H_local, 384], q|k|v along the last
+ *                      axis; q, k, v unused.
+ * Index [r, b, row, hl, :] is virtual rank r's receive slot: head r*H_local + hl
+ * of the token at global row `row` of batch row b. */
+typedef struct {
+  void* q;
+  void* k;
+  void* v;
+  void* fused;
+} qnre_out_t;
+
+/* A strided rank-4 view (device).  shape[i] >= 1 and stride[i] >= 1 are in
+ * elements; element (a, b, c, d) lives at data + (a*stride[0] + b*stride[1] +
+ * c*stride[2] + d*stride[3]) * element_size. */
+typedef struct {
+  void* data;
+  int64_t shape[4];
+  int64_t stride[4];
+  int32_t dtype; /* qnre_dtype_t */
+} qnre_tensor4_t;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* qnre_status_string(qnre_status_t status);
+
+/*
+ * qnre_plan_create -- prepare the fused QKV projection + RMSNorm + RoPE + head-band
+ * scatter for one geometry.  [FUSED] constructor: hidden = num_heads*head_dim, a
+ * multiple of 64; num_heads divisible by the world size (P here); head_dim = 128;
+ * bf16 only; max_tokens = the largest B*S_local of any call.
+ *
+ *   plan       out: receives the plan handle (host object).  Unchanged on error.
+ *   hidden     model width; must equal num_heads*128.
+ *   num_heads  attention heads H (>= 1, H % P == 0).
+ *   head_dim   must be 128 (else QNRE_ERR_UNSUPPORTED).
+ *   P          virtual Ulysses ranks (>= 1).
+ *   layout     QNRE_LAYOUT_BSHD or QNRE_LAYOUT_FUSED.
+ *   max_tokens largest B*S_local per rank accepted by qnre_forward (>= 1).
+ *   rope_style QNRE_ROPE_ROTATE_HALF or QNRE_ROPE_INTERLEAVED.
+ *   flags      0 or QNRE_FLAG_EPILOGUE_OFF.
+ *
+ * Binds to the current CUDA device: queries it, sets the kernel's shared-memory
+ * limit, and allocates the plan's 16-byte device status word (the only device
+ * allocation the library makes; it is released by qnre_plan_destroy).
+ * Errors: QNRE_ERR_INVALID_ARG, QNRE_ERR_UNSUPPORTED, QNRE_ERR_CUDA (no device,
+ * not an sm_103 GPU).
+ */
+qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int head_dim, int P,
+                               qnre_layout_t layout, int64_t max_tokens, qnre_rope_t rope_style,
+                               unsigned flags);
+
+/* Release a plan.  The caller must make sure no launched forward still runs.
+ * NULL is accepted (no-op). */
+qnre_status_t qnre_plan_destroy(qnre_plan_t plan);
+
+/*
+ * qnre_forward -- the fused op on all P virtual ranks at once.  [FUSED], [MATH]:
+ *   Y = x W (bf16 operands, fp32 accumulation) with W's columns grouped
+ *   Q | K | V (column g*H*128 + h*128 + d);
+ *   q, k heads: n_d = Y_d / sqrt(mean_d Y^2 + 1e-6) * w_{q|k}[d]  (fp32),
+ *   then RoPE with the token's cos/sin row (fp32); v heads: Y unchanged;
+ *   one rounding to bf16, stored to rank h / H_local, local head h % H_local,
+ *   global row r_s*S_local + s, for the token at (r_s, b, s).
+ *
+ *   plan      from qnre_plan_create.
+ *   B, S_local batch rows and tokens per rank; B*S_local <= max_tokens.
+ *             B*S_local == 0 is an empty call: QNRE_OK, nothing launched.
+ *   x         device bf16 [P, B, S_local, hidden] (rank r_s's shard first), 16-B aligned.
+ *   w_qkv     device bf16 [hidden, 3*H*128] row-major, 16-B aligned.
+ *   q_norm_w, k_norm_w  device bf16 [128] each, 16-B aligned.
+ *   cos_sin   device fp32 [n_pos, 128], row p = [cos_0..cos_63 | sin_0..sin_63], 16-B aligned.
+ *   n_pos     rows of cos_sin (>= 1).
+ *   positions device int32 [P, B, S_local] cos/sin row of every token, or NULL for
+ *             row = token index in [P, B, S_local] order.  A position outside
+ *             [0, n_pos) is a device-side error: that token's q and k rows are
+ *             written as NaN and QNRE_DEVICE_BAD_POSITION is raised.
+ *   out       host pointer to the output buffers (see qnre_out_t); outputs must not
+ *             overlap x, w_qkv, the norm weights, cos_sin or positions.
+ *   stream    CUDA stream.
+ *
+ * Every output element is written exactly once.  Device-side errors do not
+ * surface in the return value (the call does not wait); read them with
+ * qnre_plan_device_status.
+ */
+qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+                           const void* q_norm_w, const void* k_norm_w, const float* cos_sin,
+                           int64_t n_pos, const int32_t* positions, const qnre_out_t* out,
+                           qnre_stream_t stream);
+
+/* Read (and, if clear != 0, reset) the plan's device status bits
+ * (QNRE_DEVICE_*).  Waits for `stream`, then copies 4 bytes to the host.
+ * Returns QNRE_ERR_DEVICE when any bit is set, QNRE_OK otherwise. */
+qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, unsigned* bits,
+                                      int clear);
+
+/*
+ * ulysses_pack_head_chunk -- [PACK]: select local head band
+ * [head_offset, head_offset + head_count) inside every destination rank's
+ * H/world_size head slice of q, k and v, fusing q|k|v along the last axis:
+ *
+ *   out[b, s, r*head_count + j, c*D + d] = X_c[b, s, r*(H/world_size) + head_offset + j, d]
+ *   for X_0 = q, X_1 = k, X_2 = v, r < world_size, j < head_count.
+ *
+ *   q, k, v     host pointers to views [B, S_local, H, D] with positive strides, equal
+ *               shapes and dtype (bf16, fp16 or fp32); they may overlap each other
+ *               (e.g. slices of one fused projection buffer).
+ *   world_size  >= 1, H % world_size == 0.
+ *   head_offset, head_count  0 <= head_offset, head_count >= 1,
+ *               head_offset + head_count <= H/world_size.
+ *   out         device, contiguous [B, S_local, world_size*head_count, 3*D] of the
+ *               same dtype; must not overlap the storage range of q, k or v.
+ *   stream      CUDA stream.
+ *
+ * Element-size-aligned pointers are required (QNRE_ERR_ALIGNMENT otherwise);
+ * 16-byte aligned rows with unit innermost stride take the vectorised path.
+ * Offsets are 64-bit, so the pages' int32 payload limit ([PR5027]) does not
+ * apply.  B*S_local == 0 is an empty call (QNRE_OK, nothing launched).
+ */
+qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                                      const qnre_tensor4_t* v, int world_size, int head_offset,
+                                      int head_count, void* out, qnre_stream_t stream);
+
+/*
+ * ulysses_merge_output_head_chunk -- [MERGE]: write one gathered output head band
+ * into the full output, leaving every other element untouched:
+ *
+ *   out[b, s, r*local_heads + head_offset + j, d] = received[b, s, r*head_count + j, d]
+ *   for r < world_size, j < head_count = received.shape[2] / world_size.
+ *
+ *   received    host pointer to a view [B, S_local, world_size*head_count, D] with
+ *               positive strides (the pages' input is contiguous; any positive
+ *               strides are accepted).
+ *   world_size  >= 1, divides received.shape[2].
+ *   local_heads heads per rank in out (>= 1).
+ *   head_offset 0 <= head_offset, head_offset + head_count <= local_heads.
+ *   out         device, contiguous [B, S_local, world_size*local_heads, D] of the same
+ *               dtype; must not overlap received's storage range.
+ *   stream      CUDA stream.
+ *
+ * Same alignment, vectorisation and int32 rules as ulysses_pack_head_chunk.
+ */
+qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size,
+                                              int local_heads, int head_offset, void* out,
+                                              qnre_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* QNRE_H_ */

@@ -193,17 +193,19 @@ def place_bands(O: np.ndarray, P: int, B: int, S: int, num_heads: int,
 
     bshd : {"q","k","v"}: [P, B, S_global, H_local, D]
     fused: {"fused"}:     [P, B, S_global, H_local, 3*D], q|k|v in the last axis.
-    Unwritten elements stay NaN, so a hole in the map is visible.
+    The result has O's dtype.  Unwritten elements stay NaN (float) or all-ones
+    (integer bit patterns), so a hole in the map is visible.
     """
     if num_heads % P:
         raise ValueError("num_heads must be divisible by P")
     H_local = num_heads // P
     S_g = P * S
     D = O.shape[-1]
+    fill = np.nan if np.issubdtype(O.dtype, np.floating) else np.iinfo(O.dtype).max
     if layout == "bshd":
-        out = {g: np.full((P, B, S_g, H_local, D), np.nan) for g in "qkv"}
+        out = {g: np.full((P, B, S_g, H_local, D), fill, dtype=O.dtype) for g in "qkv"}
     elif layout == "fused":
-        out = {"fused": np.full((P, B, S_g, H_local, 3 * D), np.nan)}
+        out = {"fused": np.full((P, B, S_g, H_local, 3 * D), fill, dtype=O.dtype)}
     else:
         raise ValueError(f"unknown layout {layout!r}")
     for r_s in range(P):

@@ -1,0 +1,229 @@
+"""GPU parity of the fused QKV projection + RMSNorm + RoPE + band scatter against the oracle.
+
+Values: |gpu - oracle| <= max(2 bf16 ulp(oracle), 2e-2) per element.
+Placement: bit-exact, checked with integer-coded inputs (QNRE_FLAG_EPILOGUE_OFF)
+whose projection is exact in every precision.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from ulysses_qkv_proj_gb300 import workloads as WL
+from _util import assert_fused_close, dest_index, sample_tokens, to_dev_bf16, to_host_bits, to_host_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from ulysses_qkv_proj_gb300 import binding as qb  # noqa: E402
+
+
+def _dev_inputs(inp):
+    return dict(x=to_dev_bf16(inp.x), w=to_dev_bf16(inp.w), qw=to_dev_bf16(inp.q_norm_w),
+                kw=to_dev_bf16(inp.k_norm_w), cs=torch.from_numpy(inp.cos_sin).cuda(),
+                pos=torch.from_numpy(inp.positions).cuda())
+
+
+def _run(wl, d, flags=0, positions="given", poison=True, stream=None):
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S,
+                   rope_style=wl.rope_style, flags=flags)
+    out = qb.alloc_outputs(plan, wl.B, wl.S)
+    if poison:
+        for t in out.values():
+            t.view(torch.int16).fill_(-1)  # 0xFFFF: a NaN; every element must be rewritten
+    pos = d["pos"] if positions == "given" else None
+    qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], pos, out, stream=stream)
+    torch.cuda.synchronize()
+    status = plan.device_status()
+    return plan, out, status
+
+
+def _full_compare(wl, inp, out, positions=None):
+    ref = oracle.qnre_forward(inp.x, inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin,
+                              inp.positions if positions is None else positions,
+                              wl.P, wl.num_heads, wl.layout, wl.rope_style)
+    for g in ref:
+        assert_fused_close(to_host_f64(out[g]), ref[g], what=f"{wl.name}/{g}")
+
+
+def _wl(name, P, B, S, H, layout="bshd", rope="rotate_half"):
+    return WL.FusedWorkload(name, P=P, B=B, S=S, num_heads=H, layout=layout, rope_style=rope)
+
+
+def test_tiny_workload_full():
+    wl = WL.FUSED_WORKLOADS["tiny_p2_s64_h4"]
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    _full_compare(wl, inp, out)
+
+
+@pytest.mark.parametrize("layout", ["bshd", "fused"])
+@pytest.mark.parametrize("rope", ["rotate_half", "interleaved"])
+def test_ragged_multi_tile(layout, rope):
+    # 800 tokens = 6.25 row tiles, segments of 200 straddle tile edges; 6 column tiles.
+    wl = _wl("ragged", P=2, B=2, S=200, H=4, layout=layout, rope=rope)
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    _full_compare(wl, inp, out)
+
+
+def test_odd_head_count_column_tail():
+    # 3 heads -> N = 1152 = 4.5 tiles of 256 columns; P = 3 ranks of one head each.
+    wl = _wl("oddh", P=3, B=1, S=50, H=3)
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    _full_compare(wl, inp, out)
+
+
+def test_single_rank_and_many_ranks():
+    for wl in (_wl("p1", P=1, B=3, S=70, H=2), _wl("p8", P=8, B=1, S=16, H=8, layout="fused")):
+        inp = WL.make_fused_inputs(wl)
+        _, out, status = _run(wl, _dev_inputs(inp))
+        assert status == 0
+        _full_compare(wl, inp, out)
+
+
+def test_null_positions_use_token_index():
+    wl = _wl("nullpos", P=2, B=2, S=40, H=2)
+    inp = WL.make_fused_inputs(wl)
+    inp.cos_sin = WL.rope_table(wl.T)  # rows for every token index
+    _, out, status = _run(wl, _dev_inputs(inp), positions=None)
+    assert status == 0
+    _full_compare(wl, inp, out, positions=np.arange(wl.T))
+
+
+def test_bad_position_gives_nan_rows_and_status():
+    wl = _wl("badpos", P=2, B=1, S=64, H=2)
+    inp = WL.make_fused_inputs(wl)
+    inp.positions = inp.positions.copy()
+    inp.positions.reshape(-1)[[5, 70]] = [wl.n_pos, -3]
+    plan, out, status = _run(wl, _dev_inputs(inp))
+    assert status & qb.DEVICE_BAD_POSITION
+    assert plan.device_status() == 0  # cleared by the first read
+    _full_compare(wl, inp, out)        # NaN rows where the oracle has NaN, values elsewhere
+
+
+def _exact_projection(x2, w_bits):
+    """Closed form of x W for rows with one or two nonzeros: a sum of scaled W rows."""
+    rows, cols = np.nonzero(x2)
+    T = x2.shape[0]
+    count = np.bincount(rows, minlength=T)
+    assert count.min() >= 1 and count.max() <= 2
+    first = np.searchsorted(rows, np.arange(T))
+    second = np.minimum(first + 1, len(rows) - 1)
+    v1 = oracle.bf16_to_f64(x2[rows[first], cols[first]]).astype(np.float32)
+    v2 = np.where(count == 2, oracle.bf16_to_f64(x2[rows[second], cols[second]]), 0).astype(np.float32)
+    wf = oracle.bf16_to_f64(w_bits).astype(np.float32)
+    return wf[cols[first]] * v1[:, None] + wf[cols[second]] * v2[:, None]
+
+
+def _exact_placement(wl):
+    inp = WL.make_exact_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp), flags=qb.FLAG_EPILOGUE_OFF)
+    assert status == 0
+    # exact projection: Y[t] = W[c1(t)] + W[c2(t)], integers with |y| <= 128 (exact in bf16)
+    x2 = inp.x.reshape(wl.T, wl.hidden)
+    y = _exact_projection(x2, inp.w)
+    some = np.unique(np.linspace(0, wl.T - 1, 8).astype(int))
+    assert np.array_equal(oracle.qkv_projection(x2[some], inp.w), y[some].astype(np.float64))
+    bits = WL.f32_to_bf16_bits(y)
+    assert np.array_equal(oracle.bf16_to_f64(bits), y.astype(np.float64))  # representable exactly
+    del y
+    O = bits.reshape(wl.T, 3, wl.num_heads, 128)
+    ref = oracle.place_bands(O, wl.P, wl.B, wl.S, wl.num_heads, wl.layout)
+    for g in ref:
+        got = to_host_bits(out[g])
+        assert np.array_equal(got, ref[g]), f"{wl.name}/{g}: placement differs"
+
+
+@pytest.mark.parametrize("layout", ["bshd", "fused"])
+def test_exact_placement_small(layout):
+    _exact_placement(_wl("exact", P=4, B=2, S=96, H=8, layout=layout))
+
+
+def test_capacity_and_empty_call():
+    wl = _wl("cap", P=2, B=1, S=32, H=2)
+    inp = WL.make_fused_inputs(wl)
+    d = _dev_inputs(inp)
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, "bshd", max_tokens=16)
+    out = qb.alloc_outputs(plan, 1, 32)
+    with pytest.raises(qb.QnreError) as e:
+        qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out)
+    assert e.value.status == 5
+    empty = d["x"][:, :, :0]
+    for t in out.values():
+        t.view(torch.int16).fill_(7)
+    qb.qnre_forward(plan, empty, d["w"], d["qw"], d["kw"], d["cs"], None, out)
+    torch.cuda.synchronize()
+    for t in out.values():
+        assert bool((t.view(torch.int16) == 7).all())
+
+
+def test_output_alias_rejected():
+    wl = _wl("alias", P=2, B=1, S=32, H=2)
+    inp = WL.make_fused_inputs(wl)
+    d = _dev_inputs(inp)
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, "bshd", max_tokens=32)
+    out = qb.alloc_outputs(plan, 1, 32)
+    out["k"] = out["q"]
+    with pytest.raises(qb.QnreError) as e:
+        qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out)
+    assert e.value.status == 4
+
+
+def test_side_stream_and_two_plans():
+    wl1 = _wl("s1", P=2, B=1, S=128, H=4)
+    wl2 = _wl("s2", P=4, B=1, S=64, H=8, layout="fused", rope="interleaved")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    res = []
+    for wl in (wl1, wl2):
+        inp = WL.make_fused_inputs(wl)
+        d = _dev_inputs(inp)
+        torch.cuda.synchronize()
+        plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
+        out = qb.alloc_outputs(plan, wl.B, wl.S)
+        with torch.cuda.stream(s):
+            qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out, stream=s)
+        res.append((wl, inp, plan, out))
+    s.synchronize()
+    for wl, inp, plan, out in res:
+        assert plan.device_status() == 0
+        _full_compare(wl, inp, out)
+
+
+# ---------------------------------------------------------------------------
+# The full-size workloads: sampled values against the oracle, full coverage,
+# and full bit-exact placement.
+# ---------------------------------------------------------------------------
+FULL = ["h4096_p4_s4096", "h7168_p4_s37888_fused", "h8192_p8_b2_s16384"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_values(name):
+    wl = WL.FUSED_WORKLOADS[name]
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    for t in out.values():  # every element rewritten (poisoned with NaN before)
+        assert not bool(torch.isnan(t).any())
+    tok = sample_tokens(wl.T, wl.S, n=384)
+    x2 = inp.x.reshape(wl.T, wl.hidden)
+    O = oracle.project_norm_rope(x2[tok], inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin,
+                                 inp.positions.reshape(-1)[tok], wl.num_heads, wl.rope_style)
+    idx = torch.from_numpy(dest_index(tok, wl.P, wl.B, wl.S, wl.num_heads)).cuda()
+    for gi, g in enumerate("qkv"):
+        if wl.layout == "bshd":
+            got = out[g][idx[0], idx[1], idx[2], idx[3]]
+        else:
+            got = out["fused"][idx[0], idx[1], idx[2], idx[3]][..., gi * 128:(gi + 1) * 128]
+        assert_fused_close(to_host_f64(got), O[:, gi], what=f"{name}/{g}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_exact_placement(name):
+    _exact_placement(WL.FUSED_WORKLOADS[name])

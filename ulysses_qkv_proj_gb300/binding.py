@@ -1,0 +1,203 @@
+"""ctypes binding of libqnre (include/qnre.h).  Argument marshalling only.
+
+The names follow the C ABI: `qnre_forward`, `ulysses_pack_head_chunk`,
+`ulysses_merge_output_head_chunk`, plus the `Plan` wrapper around
+`qnre_plan_create` / `qnre_plan_destroy`.  Tensors are torch CUDA tensors;
+torch supplies device memory and the current stream, nothing else.  Every
+failure status raises `QnreError`; a missing library raises at first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Dict, List, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqnre.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "qnre.h")
+
+QNRE_OK = 0
+STATUS_NAMES = {
+    0: "QNRE_OK", 1: "QNRE_ERR_INVALID_ARG", 2: "QNRE_ERR_UNSUPPORTED", 3: "QNRE_ERR_ALIGNMENT",
+    4: "QNRE_ERR_ALIAS", 5: "QNRE_ERR_CAPACITY", 6: "QNRE_ERR_CUDA", 7: "QNRE_ERR_DEVICE",
+}
+LAYOUTS = {"bshd": 0, "fused": 1}
+ROPE_STYLES = {"rotate_half": 0, "interleaved": 1}
+FLAG_EPILOGUE_OFF = 0x1
+DEVICE_BAD_POSITION = 0x1
+DEVICE_WAIT_TIMEOUT = 0x2
+HEAD_DIM = 128
+
+
+class QnreError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class _Out(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("fused", ctypes.c_void_p)]
+
+
+class _Tensor4(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("shape", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4), ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqnre.so (built by ulysses_qkv_proj_gb300.build); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqnre.so not built ({path}); run `python -m ulysses_qkv_proj_gb300.build`")
+    lib = ctypes.CDLL(path)
+    c_int, c_i64, c_vp, c_uint = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
+    lib.qnre_status_string.restype = ctypes.c_char_p
+    lib.qnre_status_string.argtypes = [c_int]
+    lib.qnre_plan_create.restype = c_int
+    lib.qnre_plan_create.argtypes = [ctypes.POINTER(c_vp), c_int, c_int, c_int, c_int, c_int, c_i64, c_int, c_uint]
+    lib.qnre_plan_destroy.restype = c_int
+    lib.qnre_plan_destroy.argtypes = [c_vp]
+    lib.qnre_forward.restype = c_int
+    lib.qnre_forward.argtypes = [c_vp, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
+                                 ctypes.POINTER(_Out), c_vp]
+    lib.qnre_plan_device_status.restype = c_int
+    lib.qnre_plan_device_status.argtypes = [c_vp, c_vp, ctypes.POINTER(c_uint), c_int]
+    lib.ulysses_pack_head_chunk.restype = c_int
+    lib.ulysses_pack_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
+    lib.ulysses_merge_output_head_chunk.restype = c_int
+    lib.ulysses_merge_output_head_chunk.argtypes = [ctypes.POINTER(_Tensor4), c_int, c_int, c_int, c_vp, c_vp]
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER) -> List[str]:
+    """Names of the functions include/qnre.h declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                      text, flags=re.M)
+
+
+def _check(status: int, where: str) -> None:
+    if status != QNRE_OK:
+        raise QnreError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+    if t.dtype not in codes:
+        raise QnreError(2, f"dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _tensor4(t) -> _Tensor4:
+    if t.dim() != 4:
+        raise QnreError(1, "expected a rank-4 view")
+    d = _Tensor4()
+    d.data = t.data_ptr()
+    for i in range(4):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    d.dtype = _dtype_code(t)
+    return d
+
+
+class Plan:
+    """qnre_plan_create / qnre_plan_destroy."""
+
+    def __init__(self, hidden: int, num_heads: int, P: int, layout: str = "bshd",
+                 max_tokens: int = 1, rope_style: str = "rotate_half", head_dim: int = HEAD_DIM,
+                 flags: int = 0):
+        lib = load_library()
+        self._handle = ctypes.c_void_p()
+        self.hidden, self.num_heads, self.P = hidden, num_heads, P
+        self.layout, self.rope_style, self.max_tokens, self.flags = layout, rope_style, max_tokens, flags
+        _check(lib.qnre_plan_create(ctypes.byref(self._handle), hidden, num_heads, head_dim, P,
+                                    LAYOUTS.get(layout, -1), max_tokens, ROPE_STYLES.get(rope_style, -1),
+                                    flags), "qnre_plan_create")
+
+    @property
+    def handle(self):
+        return self._handle
+
+    def destroy(self) -> None:
+        if self._handle:
+            _check(load_library().qnre_plan_destroy(self._handle), "qnre_plan_destroy")
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            if self._handle:
+                load_library().qnre_plan_destroy(self._handle)
+        except Exception:
+            pass
+
+    def device_status(self, clear: bool = True, stream=None) -> int:
+        bits = ctypes.c_uint(0)
+        st = load_library().qnre_plan_device_status(self._handle, _stream_ptr(stream), ctypes.byref(bits),
+                                                    1 if clear else 0)
+        if st not in (QNRE_OK, 7):
+            raise QnreError(st, "qnre_plan_device_status")
+        return bits.value
+
+
+def qnre_forward(plan: Plan, x, w_qkv, q_norm_w, k_norm_w, cos_sin, positions, out: Dict[str, object],
+                 stream=None) -> None:
+    """x: bf16 [P, B, S_local, hidden]; out: {"q","k","v"} (bshd) or {"fused"} (fused)."""
+    if x.dim() != 4 or x.shape[0] != plan.P:
+        raise QnreError(1, "qnre_forward: x must be [P, B, S_local, hidden]")
+    o = _Out(_ptr(out.get("q")), _ptr(out.get("k")), _ptr(out.get("v")), _ptr(out.get("fused")))
+    _check(load_library().qnre_forward(plan.handle, x.shape[1], x.shape[2], x.data_ptr(), w_qkv.data_ptr(),
+                                       q_norm_w.data_ptr(), k_norm_w.data_ptr(), cos_sin.data_ptr(),
+                                       cos_sin.shape[0], _ptr(positions), ctypes.byref(o),
+                                       _stream_ptr(stream)), "qnre_forward")
+
+
+def ulysses_pack_head_chunk(q, k, v, world_size: int, head_offset: int, head_count: int, out,
+                            stream=None):
+    """Pack one head band of strided q/k/v [B, S, H, D] into contiguous out [B, S, W*cnt, 3D]."""
+    tq, tk, tv = _tensor4(q), _tensor4(k), _tensor4(v)
+    _check(load_library().ulysses_pack_head_chunk(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                                  world_size, head_offset, head_count, out.data_ptr(),
+                                                  _stream_ptr(stream)), "ulysses_pack_head_chunk")
+    return out
+
+
+def ulysses_merge_output_head_chunk(received, world_size: int, local_heads: int, head_offset: int, out,
+                                    stream=None):
+    """Merge received [B, S, W*cnt, D] into band head_offset of contiguous out [B, S, W*L, D]."""
+    tr = _tensor4(received)
+    _check(load_library().ulysses_merge_output_head_chunk(ctypes.byref(tr), world_size, local_heads,
+                                                          head_offset, out.data_ptr(), _stream_ptr(stream)),
+           "ulysses_merge_output_head_chunk")
+    return out
+
+
+def alloc_outputs(plan: Plan, B: int, S_local: int, device="cuda") -> Dict[str, object]:
+    """Output buffers for qnre_forward (uninitialised bf16)."""
+    import torch
+    H_local = plan.num_heads // plan.P
+    S_g = plan.P * S_local
+    if plan.layout == "bshd":
+        return {g: torch.empty((plan.P, B, S_g, H_local, HEAD_DIM), dtype=torch.bfloat16, device=device)
+                for g in "qkv"}
+    return {"fused": torch.empty((plan.P, B, S_g, H_local, 3 * HEAD_DIM), dtype=torch.bfloat16, device=device)}

@@ -1,0 +1,447 @@
+// fused_qkv.cu -- fused QKV projection + per-head RMSNorm + RoPE + head-band
+// scatter on the sm_103a tensor cores.
+//
+// What it computes ("Fused QKV Projection + Norm + RoPE + Head Exchange",
+// flashinfer.comm API reference; operator math from "QKV projection + RMSNorm +
+// RoPE overlapped with the Ulysses head exchange", Assumptions):
+//   Y = x W, bf16 x bf16 -> fp32; W's columns grouped Q | K | V, head-major;
+//   q/k heads: RMSNorm over the 128-wide head (eps 1e-6, shared [128] weight),
+//   then RoPE from the token's fp32 cos/sin row; v heads unchanged;
+//   bf16 result of head h of token (r_s, b, s) goes to virtual rank h / H_local,
+//   local head h % H_local, global row r_s * S + s.
+//
+// How (this kernel's design, not the pages'):
+//   * persistent grid, one CTA per SM, tiles of 128 tokens x 256 columns
+//     (= 2 heads) walked in a grouped raster so concurrent CTAs share x and W
+//     panels in L2;
+//   * warp 0: one thread issues TMA loads of x (K-major) and W (N-major) into a
+//     4-stage shared-memory ring (128-byte swizzle);
+//   * warp 1: one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32
+//     accumulate in tensor memory), double-buffering the accumulator so the
+//     epilogue of tile i overlaps the main loop of tile i+1;
+//   * warps 2-5: epilogue; thread i owns TMEM lane i = token row i of the tile,
+//     so a head's 128 values are thread-local: the RMS sum, the scale and both
+//     RoPE pairings need no cross-thread traffic; each thread then writes its
+//     head row (256 contiguous bytes) straight to the band destination.
+//   * every mbarrier wait has a time limit; on expiry the kernel raises a
+//     status bit, drains its own in-flight copies and MMAs, frees its tensor
+//     memory and returns.
+#include "fused_qkv.cuh"
+#include "ptx.cuh"
+#include "../../include/qnre.h"
+
+#include <cuda_bf16.h>
+
+namespace qnre {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kBN, /*b_mn_major=*/true);
+
+struct SmemLayout {
+  uint32_t a;      // kStages x kABytes
+  uint32_t b;      // kStages x kBBytes
+  uint32_t full;   // kStages mbarriers: TMA -> MMA
+  uint32_t empty;  // kStages mbarriers: MMA -> TMA
+  uint32_t tfull;  // 2 mbarriers: MMA -> epilogue
+  uint32_t tempty; // 2 mbarriers: epilogue -> MMA
+  uint32_t drain;  // 1 mbarrier: MMA completion on abort
+};
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag, unsigned* status,
+                                             bool honour_abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        atomicOr(status, QNRE_DEVICE_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tile_coords(int tile, const FusedArgs& a, int& m_blk, int& n_blk) {
+  const int per_group = a.group_m * a.num_n_tiles;
+  const int group = tile / per_group;
+  const int first_m = group * a.group_m;
+  const int gm = min(a.group_m, a.num_m_tiles - first_m);
+  const int within = tile - group * per_group;
+  m_blk = first_m + within % gm;
+  n_blk = within / gm;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Compiler-level barrier: the registers count as rewritten here, so no use of
+// them is scheduled above the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
+__device__ __forceinline__ void rotate(float& a, float& b, float c, float s) {
+  const float na = a * c - b * s;
+  const float nb = b * c + a * s;
+  a = na;
+  b = nb;
+}
+
+// --------------------------------------------------------------------------
+// Producer: TMA loads of the x and W tiles into the stage ring.
+// --------------------------------------------------------------------------
+__device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile uint32_t* abort_flag) {
+  uint32_t g = 0;
+  uint32_t used_mask = 0, parity_mask = 0;  // per stage: ever loaded / parity of its last load
+  const uint64_t pol_w = ptx::l2_policy_evict_last();
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+    int m_blk, n_blk;
+    tile_coords(tile, a, m_blk, n_blk);
+    for (int kb = 0; kb < a.num_k_blocks; ++kb, ++g) {
+      const uint32_t s = g % kStages;
+      const uint32_t ph = (g / kStages) & 1u;
+      if (!bounded_wait(L.empty + 8 * s, ph ^ 1u, abort_flag, a.status, true)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = L.full + 8 * s;
+      ptx::mbar_arrive_expect_tx(full, kABytes + kBBytes);
+      ptx::tma_load_2d(L.a + s * kABytes, &a.tmap_x, full, kb * kBK, m_blk * kBM);
+#pragma unroll
+      for (int j = 0; j < kBN / 64; ++j) {
+        ptx::tma_load_2d_hint(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, full,
+                              n_blk * kBN + j * 64, kb * kBK, pol_w);
+      }
+      used_mask |= 1u << s;
+      parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
+    }
+  }
+  if (!ok) {
+    // Abort: let every load already issued land before the CTA can exit.
+    for (uint32_t s = 0; s < kStages; ++s) {
+      if (used_mask & (1u << s)) {
+        bounded_wait(L.full + 8 * s, (parity_mask >> s) & 1u, abort_flag, a.status, false);
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// MMA issuer: tcgen05.mma over the stage ring into the TMEM accumulators.
+// --------------------------------------------------------------------------
+__device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
+                        volatile uint32_t* abort_flag) {
+  uint32_t g = 0;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++it) {
+    const uint32_t acc = it & 1u;
+    const uint32_t aph = (it >> 1) & 1u;
+    if (!bounded_wait(L.tempty + 8 * acc, aph ^ 1u, abort_flag, a.status, true)) {
+      ok = false;
+      break;
+    }
+    ptx::tc_fence_after_sync();
+    const uint32_t d_tmem = tmem_base + acc * kAccCols;
+    for (int kb = 0; kb < a.num_k_blocks; ++kb, ++g) {
+      const uint32_t s = g % kStages;
+      const uint32_t ph = (g / kStages) & 1u;
+      if (!bounded_wait(L.full + 8 * s, ph, abort_flag, a.status, true)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+      const uint32_t a_base = L.a + s * kABytes;
+      const uint32_t b_base = L.b + s * kBBytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        // A: K-major, rows of 128 B (64 bf16), 8-row groups 1024 B apart;
+        //    the k-th 16-wide slice starts 32 B into the swizzled row.
+        const uint64_t adesc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+        // B: N-major, 64-column blocks of kBK rows x 128 B (LBO = 8 KiB apart),
+        //    8-row k groups 1024 B apart; the k-th 16-row slice starts 2 KiB in.
+        const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024);
+        ptx::umma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(L.empty + 8 * s);  // frees the stage once these MMAs finish
+    }
+    if (!ok) break;
+    ptx::umma_commit(L.tfull + 8 * acc);  // accumulator ready for the epilogue
+  }
+  if (!ok) {
+    ptx::umma_commit(L.drain);
+    bounded_wait(L.drain, 0, abort_flag, a.status, false);
+  }
+}
+
+// --------------------------------------------------------------------------
+// Epilogue: TMEM -> registers -> norm / RoPE -> bf16 -> band destination.
+// --------------------------------------------------------------------------
+__device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
+                             const float* norm_w, volatile uint32_t* abort_flag) {
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int sub = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = sub * 32 + lane;
+  const int S_g = a.P * a.S;
+  const int three_h = 3 * a.H;
+  uint32_t it = 0;
+  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++it) {
+    const uint32_t acc = it & 1u;
+    const uint32_t aph = (it >> 1) & 1u;
+    if (!bounded_wait(L.tfull + 8 * acc, aph, abort_flag, a.status, true)) break;
+    ptx::tc_fence_after_sync();
+
+    int m_blk, n_blk;
+    tile_coords(tile, a, m_blk, n_blk);
+    const int t = m_blk * kBM + row;
+    const bool valid = t < a.T;
+    const int s_loc = valid ? t % a.S : 0;
+    const int tb = valid ? t / a.S : 0;
+    const int b = tb % a.B;
+    const int r_s = tb / a.B;
+    long long pos = 0;
+    bool bad_pos = false;
+    if (valid && a.epilogue_on) {
+      pos = a.positions != nullptr ? static_cast<long long>(a.positions[t]) : static_cast<long long>(t);
+      bad_pos = pos < 0 || pos >= a.n_pos;
+    }
+    const long long dest_row = static_cast<long long>(r_s) * a.S + s_loc;  // global row in batch b
+
+#pragma unroll 1
+    for (int hh = 0; hh < kBN / 128; ++hh) {
+      const int ch = n_blk * (kBN / 128) + hh;  // head column index in [0, 3H)
+      if (ch >= three_h) break;
+      const int g = ch / a.H;
+      const int h = ch - g * a.H;
+      const int r = h / a.H_local;
+      const int hl = h - r * a.H_local;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * kAccCols + hh * 128;
+      uint16_t* dst;
+      if (a.layout == 0) {
+        uint16_t* base = g == 0 ? a.out_q : (g == 1 ? a.out_k : a.out_v);
+        dst = base + ((((static_cast<long long>(r) * a.B + b) * S_g + dest_row) * a.H_local + hl) * 128);
+      } else {
+        dst = a.out_fused +
+              ((((static_cast<long long>(r) * a.B + b) * S_g + dest_row) * a.H_local + hl) * 384 + g * 128);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      const bool normed = g < 2 && a.epilogue_on;
+
+      // Pass 1 (q, k): mean square of the head row.
+      float scale = 1.0f;
+      if (normed) {
+        float ss = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld_32x32b_x32(taddr + half * 64, r0);
+          ptx::tmem_ld_32x32b_x32(taddr + half * 64 + 32, r1);
+          ptx::tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x0 = __uint_as_float(r0[i]);
+            const float x1 = __uint_as_float(r1[i]);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+          }
+        }
+        scale = rsqrtf(ss * (1.0f / 128.0f) + 1e-6f);
+      }
+      const float* wn = norm_w + (g < 2 ? g : 0) * 128;
+      const float4* cs = reinterpret_cast<const float4*>(a.cos_sin + pos * 128);
+      const bool nan_out = normed && bad_pos;
+      const bool rope = normed && !bad_pos;
+
+      // Pass 2: scale, rotate, round, store.  Work on 64 columns at a time:
+      // rotate-half pairs column i with i + 64, so step p takes columns
+      // [32p, 32p + 32) and [64 + 32p, 96 + 32p); interleaved pairs are
+      // adjacent, so step p takes [64p, 64p + 64).
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const bool rh = a.rope_style == 0;
+        const int c_lo = rh ? 32 * p : 64 * p;
+        const int c_hi = rh ? 64 + 32 * p : 64 * p + 32;
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c_lo, r0);
+        ptx::tmem_ld_32x32b_x32(taddr + c_hi, r1);
+        ptx::tmem_ld_wait();
+        reg_fence(r0);
+        reg_fence(r1);
+        float lo[32], hi[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          lo[i] = __uint_as_float(r0[i]);
+          hi[i] = __uint_as_float(r1[i]);
+        }
+        if (normed) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            lo[i] = (lo[i] * scale) * wn[c_lo + i];
+            hi[i] = (hi[i] * scale) * wn[c_hi + i];
+          }
+        }
+        if (rope) {
+          if (rh) {
+            // pair (c_lo + i, c_hi + i) uses angle index 32p + i
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 c = __ldg(cs + 8 * p + i4);
+              const float4 sn = __ldg(cs + 16 + 8 * p + i4);
+              rotate(lo[4 * i4 + 0], hi[4 * i4 + 0], c.x, sn.x);
+              rotate(lo[4 * i4 + 1], hi[4 * i4 + 1], c.y, sn.y);
+              rotate(lo[4 * i4 + 2], hi[4 * i4 + 2], c.z, sn.z);
+              rotate(lo[4 * i4 + 3], hi[4 * i4 + 3], c.w, sn.w);
+            }
+          } else {
+            // pairs (2i, 2i+1) over columns [64p, 64p + 64): angle index 32p + i
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 c = __ldg(cs + 8 * p + i4);
+              const float4 sn = __ldg(cs + 16 + 8 * p + i4);
+              float* v = i4 < 4 ? lo : hi;
+              const int o = (i4 & 3) * 8;
+              rotate(v[o + 0], v[o + 1], c.x, sn.x);
+              rotate(v[o + 2], v[o + 3], c.y, sn.y);
+              rotate(v[o + 4], v[o + 5], c.z, sn.z);
+              rotate(v[o + 6], v[o + 7], c.w, sn.w);
+            }
+          }
+        }
+        if (nan_out) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            lo[i] = __uint_as_float(0x7FC00000u);
+            hi[i] = __uint_as_float(0x7FC00000u);
+          }
+        }
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 u;
+            u.x = pack_bf16x2(lo[8 * j + 0], lo[8 * j + 1]);
+            u.y = pack_bf16x2(lo[8 * j + 2], lo[8 * j + 3]);
+            u.z = pack_bf16x2(lo[8 * j + 4], lo[8 * j + 5]);
+            u.w = pack_bf16x2(lo[8 * j + 6], lo[8 * j + 7]);
+            d4[c_lo / 8 + j] = u;
+            uint4 w;
+            w.x = pack_bf16x2(hi[8 * j + 0], hi[8 * j + 1]);
+            w.y = pack_bf16x2(hi[8 * j + 2], hi[8 * j + 3]);
+            w.z = pack_bf16x2(hi[8 * j + 4], hi[8 * j + 5]);
+            w.w = pack_bf16x2(hi[8 * j + 6], hi[8 * j + 7]);
+            d4[c_hi / 8 + j] = w;
+          }
+        }
+      }
+    }
+    if (bad_pos && valid) atomicOr(a.status, QNRE_DEVICE_BAD_POSITION);
+
+    // Hand the accumulator back to the MMA warp.
+    ptx::tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(L.tempty + 8 * acc);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_constant__ FusedArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* smem = smem_raw + pad;
+
+  SmemLayout L;
+  L.a = raw + pad;
+  L.b = L.a + kStages * kABytes;
+  const uint32_t bar0 = L.b + kStages * kBBytes;
+  L.full = bar0;
+  L.empty = L.full + 8 * kStages;
+  L.tfull = L.empty + 8 * kStages;
+  L.tempty = L.tfull + 16;
+  L.drain = L.tempty + 16;
+  uint8_t* bar_ptr = smem + kStages * (kABytes + kBBytes);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kStages + 5));
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+  float* norm_w = reinterpret_cast<float*>(bar_ptr + kBarBytes);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tensormap(&args.tmap_x);
+    ptx::prefetch_tensormap(&args.tmap_w);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(L.full + 8 * s, 1);
+      ptx::mbar_init(L.empty + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(L.tfull + 8 * i, 1);
+      ptx::mbar_init(L.tempty + 8 * i, 4);  // one arrival per epilogue warp
+    }
+    ptx::mbar_init(L.drain, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
+    ptx::tmem_relinquish_alloc_permit();
+  }
+  if (threadIdx.x >= 64) {
+    const int d = threadIdx.x - 64;  // 0..127
+    norm_w[d] = bf16_bits_to_float(args.q_norm_w[d]);
+    norm_w[128 + d] = bf16_bits_to_float(args.k_norm_w[d]);
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer(args, L, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) run_mma(args, L, tmem_base, abort_flag);
+    __syncwarp();
+  } else {
+    run_epilogue(args, L, tmem_base, norm_w, abort_flag);
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_fused_qkv_kernel() {
+  return cudaFuncSetAttribute(fused_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t launch_fused_qkv(const FusedArgs& args, int grid, cudaStream_t stream) {
+  fused_qkv_kernel<<<grid, kThreads, kSmemBytes, stream>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace qnre

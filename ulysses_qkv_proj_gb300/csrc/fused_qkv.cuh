@@ -1,0 +1,52 @@
+// fused_qkv.cuh -- kernel arguments and launcher of the fused QKV projection +
+// per-head RMSNorm + RoPE + head-band scatter (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace qnre {
+
+// Tile geometry.  One CTA owns a BM x BN tile of Y = x W: BM tokens by two
+// 128-wide heads, so the whole head row of a token is one TMEM lane.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kABytes = kBM * kBK * 2;        // 16 KiB
+constexpr int kBBytes = kBN * kBK * 2;        // 32 KiB
+constexpr int kAccCols = kBN;                 // fp32 accumulator columns per buffer
+constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator
+constexpr int kBarBytes = 256;                // mbarriers + small words
+constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kABytes + kBBytes) + kBarBytes +
+                           2 * 128 * 4 /*norm weights*/;
+
+struct FusedArgs {
+  CUtensorMap tmap_x;  // bf16 [T, K], box 64 x 128, 128-byte swizzle
+  CUtensorMap tmap_w;  // bf16 [K, N], box 64 x 64, 128-byte swizzle
+  const uint16_t* q_norm_w;
+  const uint16_t* k_norm_w;
+  const float* cos_sin;
+  const int32_t* positions;
+  uint16_t* out_q;
+  uint16_t* out_k;
+  uint16_t* out_v;
+  uint16_t* out_fused;
+  unsigned* status;
+  long long n_pos;
+  int T, K, N, H, H_local, P, B, S;
+  int layout;       // 0 bshd, 1 fused
+  int rope_style;   // 0 rotate-half, 1 interleaved
+  int epilogue_on;  // 0: bare projection
+  int num_m_tiles, num_n_tiles, num_tiles, group_m, num_k_blocks;
+};
+
+// Enqueue the fused kernel.  `grid` CTAs walk the tile list persistently.
+cudaError_t launch_fused_qkv(const FusedArgs& args, int grid, cudaStream_t stream);
+
+// One-time per-device kernel attribute setup (shared-memory opt-in).
+cudaError_t prepare_fused_qkv_kernel();
+
+}  // namespace qnre

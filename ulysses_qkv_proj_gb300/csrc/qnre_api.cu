@@ -1,0 +1,435 @@
+// qnre_api.cu -- the extern "C" boundary of libqnre: argument checks, the plan
+// object, TMA descriptor encoding and kernel launches.  Every check runs before
+// anything is enqueued, so a rejected call has no effect.
+#include "../../include/qnre.h"
+#include "fused_qkv.cuh"
+#include "head_chunk.cuh"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <new>
+
+struct qnre_plan_s {
+  int hidden = 0;
+  int num_heads = 0;
+  int P = 0;
+  int H_local = 0;
+  qnre_layout_t layout = QNRE_LAYOUT_BSHD;
+  int64_t max_tokens = 0;
+  qnre_rope_t rope_style = QNRE_ROPE_ROTATE_HALF;
+  unsigned flags = 0;
+  int device = -1;
+  int num_sms = 0;
+  unsigned* d_status = nullptr;
+};
+
+namespace {
+
+using qnre::FusedArgs;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct ByteRange {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(ByteRange a, ByteRange b) { return a.lo < b.hi && b.lo < a.hi; }
+
+ByteRange span(const void* p, uint64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+// ------------------------------------------------------------------ TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major matrix [rows, cols], box = box_cols x box_rows, 128-byte swizzle.
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int dtype_size(int32_t dt) {
+  switch (dt) {
+    case QNRE_DTYPE_BF16: return 2;
+    case QNRE_DTYPE_FP16: return 2;
+    case QNRE_DTYPE_FP32: return 4;
+    default: return 0;
+  }
+}
+
+// Checks common to every strided view; fills the byte span of its storage.
+qnre_status_t check_view(const qnre_tensor4_t* t, ByteRange* range) {
+  if (t == nullptr || t->data == nullptr) return QNRE_ERR_INVALID_ARG;
+  const int esz = dtype_size(t->dtype);
+  if (esz == 0) return QNRE_ERR_UNSUPPORTED;
+  // Batch and sequence extents may be 0 (an empty call); heads and head_dim may not.
+  bool empty = false;
+  uint64_t last = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (t->shape[i] < (i < 2 ? 0 : 1) || t->stride[i] < 1) return QNRE_ERR_INVALID_ARG;
+    if (t->shape[i] > (int64_t{1} << 40) || t->stride[i] > (int64_t{1} << 40)) return QNRE_ERR_CAPACITY;
+    if (t->shape[i] == 0) {
+      empty = true;
+      continue;
+    }
+    last += static_cast<uint64_t>(t->shape[i] - 1) * static_cast<uint64_t>(t->stride[i]);
+    if (last > (uint64_t{1} << 56)) return QNRE_ERR_CAPACITY;
+  }
+  if (!aligned(t->data, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
+  *range = empty ? ByteRange{0, 0} : span(t->data, (last + 1) * static_cast<uint64_t>(esz));
+  return QNRE_OK;
+}
+
+bool rows_vectorisable(const qnre_tensor4_t* t, int esz) {
+  if (t->stride[3] != 1) return false;
+  if ((t->shape[3] * esz) % 16 != 0) return false;
+  if (!aligned(t->data, 16)) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((t->stride[i] * esz) % 16 != 0) return false;
+  return true;
+}
+
+qnre_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QNRE_OK : QNRE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qnre_status_string(qnre_status_t s) {
+  switch (s) {
+    case QNRE_OK: return "QNRE_OK";
+    case QNRE_ERR_INVALID_ARG: return "QNRE_ERR_INVALID_ARG: invalid argument";
+    case QNRE_ERR_UNSUPPORTED: return "QNRE_ERR_UNSUPPORTED: unsupported configuration";
+    case QNRE_ERR_ALIGNMENT: return "QNRE_ERR_ALIGNMENT: misaligned pointer or stride";
+    case QNRE_ERR_ALIAS: return "QNRE_ERR_ALIAS: output overlaps an input";
+    case QNRE_ERR_CAPACITY: return "QNRE_ERR_CAPACITY: size beyond the plan or index limits";
+    case QNRE_ERR_CUDA: return "QNRE_ERR_CUDA: CUDA call failed";
+    case QNRE_ERR_DEVICE: return "QNRE_ERR_DEVICE: device-side check fired";
+  }
+  return "QNRE_ERR_UNKNOWN";
+}
+
+qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int head_dim, int P,
+                               qnre_layout_t layout, int64_t max_tokens, qnre_rope_t rope_style,
+                               unsigned flags) {
+  if (plan == nullptr) return QNRE_ERR_INVALID_ARG;
+  if (head_dim != QNRE_HEAD_DIM) return head_dim > 0 ? QNRE_ERR_UNSUPPORTED : QNRE_ERR_INVALID_ARG;
+  if (num_heads < 1 || P < 1 || hidden < 1) return QNRE_ERR_INVALID_ARG;
+  if (hidden != num_heads * head_dim || hidden % 64 != 0) return QNRE_ERR_INVALID_ARG;
+  if (num_heads % P != 0) return QNRE_ERR_INVALID_ARG;
+  if (layout != QNRE_LAYOUT_BSHD && layout != QNRE_LAYOUT_FUSED) return QNRE_ERR_INVALID_ARG;
+  if (rope_style != QNRE_ROPE_ROTATE_HALF && rope_style != QNRE_ROPE_INTERLEAVED) return QNRE_ERR_INVALID_ARG;
+  if ((flags & ~QNRE_FLAG_EPILOGUE_OFF) != 0) return QNRE_ERR_INVALID_ARG;
+  if (max_tokens < 1) return QNRE_ERR_INVALID_ARG;
+  // The kernel's tile indices and TMA coordinates are 32-bit.
+  if (max_tokens * static_cast<int64_t>(P) > (int64_t{1} << 31) - 256) return QNRE_ERR_CAPACITY;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QNRE_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QNRE_ERR_CUDA;
+  if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
+  if (qnre::prepare_fused_qkv_kernel() != cudaSuccess) return QNRE_ERR_CUDA;
+  if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
+
+  qnre_plan_s* p = new (std::nothrow) qnre_plan_s();
+  if (p == nullptr) return QNRE_ERR_CUDA;
+  if (cudaMalloc(&p->d_status, 16) != cudaSuccess) {
+    delete p;
+    return QNRE_ERR_CUDA;
+  }
+  if (cudaMemset(p->d_status, 0, 16) != cudaSuccess) {
+    cudaFree(p->d_status);
+    delete p;
+    return QNRE_ERR_CUDA;
+  }
+  p->hidden = hidden;
+  p->num_heads = num_heads;
+  p->P = P;
+  p->H_local = num_heads / P;
+  p->layout = layout;
+  p->max_tokens = max_tokens;
+  p->rope_style = rope_style;
+  p->flags = flags;
+  p->device = dev;
+  p->num_sms = sms;
+  *plan = p;
+  return QNRE_OK;
+}
+
+qnre_status_t qnre_plan_destroy(qnre_plan_t plan) {
+  if (plan == nullptr) return QNRE_OK;
+  cudaError_t e = cudaSuccess;
+  if (plan->d_status != nullptr) e = cudaFree(plan->d_status);
+  delete plan;
+  return from_cuda(e);
+}
+
+qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+                           const void* q_norm_w, const void* k_norm_w, const float* cos_sin, int64_t n_pos,
+                           const int32_t* positions, const qnre_out_t* out, qnre_stream_t stream) {
+  if (plan == nullptr || out == nullptr) return QNRE_ERR_INVALID_ARG;
+  if (B < 0 || S_local < 0) return QNRE_ERR_INVALID_ARG;
+  const int64_t tokens_per_rank = static_cast<int64_t>(B) * S_local;
+  if (tokens_per_rank > plan->max_tokens) return QNRE_ERR_CAPACITY;
+  if (tokens_per_rank == 0) return QNRE_OK;
+  if (x == nullptr || w_qkv == nullptr || q_norm_w == nullptr || k_norm_w == nullptr || cos_sin == nullptr)
+    return QNRE_ERR_INVALID_ARG;
+  if (n_pos < 1) return QNRE_ERR_INVALID_ARG;
+  const bool bshd = plan->layout == QNRE_LAYOUT_BSHD;
+  if (bshd ? (out->q == nullptr || out->k == nullptr || out->v == nullptr) : out->fused == nullptr)
+    return QNRE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_qkv, 16) || !aligned(q_norm_w, 16) || !aligned(k_norm_w, 16) ||
+      !aligned(cos_sin, 16) || (positions != nullptr && !aligned(positions, 4)))
+    return QNRE_ERR_ALIGNMENT;
+  if (bshd ? (!aligned(out->q, 16) || !aligned(out->k, 16) || !aligned(out->v, 16)) : !aligned(out->fused, 16))
+    return QNRE_ERR_ALIGNMENT;
+
+  const int P = plan->P;
+  const int64_t T = tokens_per_rank * P;
+  const int64_t K = plan->hidden;
+  const int64_t N = 3 * K;
+  if (n_pos > (int64_t{1} << 40)) return QNRE_ERR_CAPACITY;
+
+  // Storage ranges: outputs must not overlap any input, nor each other.
+  const uint64_t band_bytes = static_cast<uint64_t>(T) * K * 2;  // one of q/k/v over all ranks
+  const ByteRange in[6] = {span(x, static_cast<uint64_t>(T) * K * 2), span(w_qkv, static_cast<uint64_t>(K) * N * 2),
+                           span(q_norm_w, 256), span(k_norm_w, 256),
+                           span(cos_sin, static_cast<uint64_t>(n_pos) * 512),
+                           positions ? span(positions, static_cast<uint64_t>(T) * 4) : ByteRange{0, 0}};
+  ByteRange outs[3];
+  int n_out = 0;
+  if (bshd) {
+    outs[n_out++] = span(out->q, band_bytes);
+    outs[n_out++] = span(out->k, band_bytes);
+    outs[n_out++] = span(out->v, band_bytes);
+  } else {
+    outs[n_out++] = span(out->fused, 3 * band_bytes);
+  }
+  for (int i = 0; i < n_out; ++i) {
+    for (const ByteRange& r : in)
+      if (r.hi > r.lo && overlaps(outs[i], r)) return QNRE_ERR_ALIAS;
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlaps(outs[i], outs[j])) return QNRE_ERR_ALIAS;
+  }
+
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return QNRE_ERR_CUDA;
+  if (cur != plan->device) return QNRE_ERR_INVALID_ARG;
+
+  FusedArgs a;
+  if (!encode_2d_bf16(&a.tmap_x, x, static_cast<uint64_t>(T), static_cast<uint64_t>(K), qnre::kBK, qnre::kBM))
+    return QNRE_ERR_CUDA;
+  if (!encode_2d_bf16(&a.tmap_w, w_qkv, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 64, qnre::kBK))
+    return QNRE_ERR_CUDA;
+  a.q_norm_w = static_cast<const uint16_t*>(q_norm_w);
+  a.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
+  a.cos_sin = cos_sin;
+  a.positions = positions;
+  a.out_q = static_cast<uint16_t*>(bshd ? out->q : nullptr);
+  a.out_k = static_cast<uint16_t*>(bshd ? out->k : nullptr);
+  a.out_v = static_cast<uint16_t*>(bshd ? out->v : nullptr);
+  a.out_fused = static_cast<uint16_t*>(bshd ? nullptr : out->fused);
+  a.status = plan->d_status;
+  a.n_pos = n_pos;
+  a.T = static_cast<int>(T);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.H = plan->num_heads;
+  a.H_local = plan->H_local;
+  a.P = P;
+  a.B = B;
+  a.S = S_local;
+  a.layout = bshd ? 0 : 1;
+  a.rope_style = plan->rope_style == QNRE_ROPE_INTERLEAVED ? 1 : 0;
+  a.epilogue_on = (plan->flags & QNRE_FLAG_EPILOGUE_OFF) ? 0 : 1;
+  const int64_t m_tiles = (T + qnre::kBM - 1) / qnre::kBM;
+  const int64_t n_tiles = (N + qnre::kBN - 1) / qnre::kBN;
+  if (m_tiles * n_tiles > INT32_MAX) return QNRE_ERR_CAPACITY;
+  a.num_m_tiles = static_cast<int>(m_tiles);
+  a.num_n_tiles = static_cast<int>(n_tiles);
+  a.num_tiles = a.num_m_tiles * a.num_n_tiles;
+  a.group_m = std::min(a.num_m_tiles, 16);
+  a.num_k_blocks = static_cast<int>(K / qnre::kBK);
+  const int grid = std::min(a.num_tiles, plan->num_sms);
+  return from_cuda(qnre::launch_fused_qkv(a, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, unsigned* bits, int clear) {
+  if (plan == nullptr || bits == nullptr) return QNRE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QNRE_ERR_CUDA;
+  if (cudaMemcpy(&host, plan->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QNRE_ERR_CUDA;
+  if (clear && cudaMemset(plan->d_status, 0, sizeof(unsigned)) != cudaSuccess) return QNRE_ERR_CUDA;
+  *bits = host;
+  return host ? QNRE_ERR_DEVICE : QNRE_OK;
+}
+
+qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const qnre_tensor4_t* v,
+                                      int world_size, int head_offset, int head_count, void* out,
+                                      qnre_stream_t stream) {
+  const qnre_tensor4_t* X[3] = {q, k, v};
+  ByteRange in[3];
+  for (int c = 0; c < 3; ++c) {
+    const qnre_status_t st = check_view(X[c], &in[c]);
+    if (st != QNRE_OK) return st;
+  }
+  for (int c = 1; c < 3; ++c) {
+    if (X[c]->dtype != q->dtype) return QNRE_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+      if (X[c]->shape[i] != q->shape[i]) return QNRE_ERR_INVALID_ARG;
+  }
+  if (out == nullptr) return QNRE_ERR_INVALID_ARG;
+  const int64_t B = q->shape[0], S = q->shape[1], H = q->shape[2], D = q->shape[3];
+  if (world_size < 1 || H % world_size != 0) return QNRE_ERR_INVALID_ARG;
+  const int64_t H_local = H / world_size;
+  if (head_offset < 0 || head_count < 1 || head_offset + static_cast<int64_t>(head_count) > H_local)
+    return QNRE_ERR_INVALID_ARG;
+  if (B > 65535) return QNRE_ERR_CAPACITY;
+  const int esz = dtype_size(q->dtype);
+  if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
+  const int64_t slots = static_cast<int64_t>(world_size) * head_count;
+  const uint64_t out_bytes = static_cast<uint64_t>(B) * S * slots * 3 * D * esz;
+  const ByteRange o = span(out, out_bytes);
+  for (int c = 0; c < 3; ++c)
+    if (overlaps(o, in[c])) return QNRE_ERR_ALIAS;
+
+  if (B == 0 || S == 0) return QNRE_OK;  // empty call
+  const bool vec = aligned(out, 16) && rows_vectorisable(q, esz) && rows_vectorisable(k, esz) &&
+                   rows_vectorisable(v, esz);
+  qnre::SegCopyPlan p{};
+  for (int c = 0; c < 3; ++c) {
+    p.src[c] = X[c]->data;
+    p.src_sb[c] = X[c]->stride[0] * esz;
+    p.src_ss[c] = X[c]->stride[1] * esz;
+    p.src_sh[c] = X[c]->stride[2] * esz;
+  }
+  p.unit_bytes = vec ? 16 : esz;
+  p.units = static_cast<int>(vec ? D * esz / 16 : D);
+  p.src_sd = vec ? 16 : q->stride[3] * esz;
+  // k and v must share q's innermost stride on the element path.
+  if (!vec && (k->stride[3] != q->stride[3] || v->stride[3] != q->stride[3])) {
+    // Fall back to one launch per component with its own stride.
+    for (int c = 0; c < 3; ++c) {
+      qnre::SegCopyPlan pc = p;
+      pc.src[0] = X[c]->data;
+      pc.src_sb[0] = p.src_sb[c];
+      pc.src_ss[0] = p.src_ss[c];
+      pc.src_sh[0] = p.src_sh[c];
+      pc.src_sd = X[c]->stride[3] * esz;
+      pc.dst = static_cast<char*>(out) + static_cast<int64_t>(c) * D * esz;
+      pc.dst_sb = S * slots * 3 * D * esz;
+      pc.dst_ss = slots * 3 * D * esz;
+      pc.B = B;
+      pc.S = S;
+      pc.comps = 1;
+      pc.segments = static_cast<int>(slots);
+      pc.head_count = head_count;
+      pc.src_heads_per_rank = static_cast<int>(H_local);
+      pc.src_head_offset = head_offset;
+      pc.dst_heads_per_rank = head_count;
+      pc.dst_head_offset = 0;
+      pc.dst_seg_bytes = 3 * D * esz;  // consecutive slots are 3*D elements apart
+      const cudaError_t e = qnre::launch_seg_copy(pc, reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return QNRE_ERR_CUDA;
+    }
+    return QNRE_OK;
+  }
+  p.dst = out;
+  p.dst_sb = S * slots * 3 * D * esz;
+  p.dst_ss = slots * 3 * D * esz;
+  p.B = B;
+  p.S = S;
+  p.comps = 3;
+  p.segments = static_cast<int>(slots * 3);
+  p.head_count = head_count;
+  p.src_heads_per_rank = static_cast<int>(H_local);
+  p.src_head_offset = head_offset;
+  p.dst_heads_per_rank = head_count;
+  p.dst_head_offset = 0;
+  p.dst_seg_bytes = D * esz;
+  return from_cuda(qnre::launch_seg_copy(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size, int local_heads,
+                                              int head_offset, void* out, qnre_stream_t stream) {
+  ByteRange in;
+  const qnre_status_t st = check_view(received, &in);
+  if (st != QNRE_OK) return st;
+  if (out == nullptr) return QNRE_ERR_INVALID_ARG;
+  const int64_t B = received->shape[0], S = received->shape[1], WC = received->shape[2], D = received->shape[3];
+  if (world_size < 1 || WC % world_size != 0) return QNRE_ERR_INVALID_ARG;
+  const int64_t head_count = WC / world_size;
+  if (local_heads < 1 || head_offset < 0 || head_offset + head_count > local_heads) return QNRE_ERR_INVALID_ARG;
+  if (B > 65535) return QNRE_ERR_CAPACITY;
+  const int esz = dtype_size(received->dtype);
+  if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
+  const int64_t out_heads = static_cast<int64_t>(world_size) * local_heads;
+  const ByteRange o = span(out, static_cast<uint64_t>(B) * S * out_heads * D * esz);
+  if (overlaps(o, in)) return QNRE_ERR_ALIAS;
+
+  if (B == 0 || S == 0) return QNRE_OK;  // empty call
+  const bool vec = aligned(out, 16) && rows_vectorisable(received, esz);
+  qnre::SegCopyPlan p{};
+  p.src[0] = p.src[1] = p.src[2] = received->data;
+  for (int c = 0; c < 3; ++c) {
+    p.src_sb[c] = received->stride[0] * esz;
+    p.src_ss[c] = received->stride[1] * esz;
+    p.src_sh[c] = received->stride[2] * esz;
+  }
+  p.unit_bytes = vec ? 16 : esz;
+  p.units = static_cast<int>(vec ? D * esz / 16 : D);
+  p.src_sd = vec ? 16 : received->stride[3] * esz;
+  p.dst = out;
+  p.dst_sb = S * out_heads * D * esz;
+  p.dst_ss = out_heads * D * esz;
+  p.B = B;
+  p.S = S;
+  p.comps = 1;
+  p.segments = static_cast<int>(WC);
+  p.head_count = static_cast<int>(head_count);
+  p.src_heads_per_rank = static_cast<int>(head_count);
+  p.src_head_offset = 0;
+  p.dst_heads_per_rank = local_heads;
+  p.dst_head_offset = head_offset;
+  p.dst_seg_bytes = D * esz;
+  return from_cuda(qnre::launch_seg_copy(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
