@@ -173,6 +173,47 @@ qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, un
                                       int clear);
 
 /*
+ * qnre_forward_noalloc -- qnre_forward without a plan and without any device
+ * allocation.  The pages have no counterpart: this entry point exists for
+ * callers that cannot call cudaMalloc when they run the projection (a
+ * framework whose memory pool forbids raw device allocations, a runtime that
+ * has handed all device memory to its own allocator, a server that must not
+ * allocate once it is running).  qnre_plan_create allocates the plan's device
+ * status word, so such callers cannot make a plan; this call keeps that word
+ * in a static device array of the library instead.
+ *
+ *   hidden, num_heads, P, layout, rope_style, flags
+ *             the geometry qnre_plan_create takes (head_dim is 128), with the
+ *             same rules and error codes.
+ *   B .. out  as in qnre_forward (there is no max_tokens; see the limit below).
+ *   device_status_out  device pointer to one unsigned (4-byte aligned), or NULL:
+ *             receives this call's QNRE_DEVICE_* bits, in stream order.
+ *   stream    CUDA stream.
+ *
+ * Scratch and limits: the library holds a 256-byte static device array on
+ * every GPU that loads it, until the process exits; a call uses 16 bytes of it.
+ * Sizes beyond what the call serves are rejected with QNRE_ERR_CAPACITY: a
+ * status block larger than the array, or P*B*S_local tokens beyond 2^31 - 256.
+ * The call makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and sets the kernel's
+ * shared-memory limit.  Make that first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array.  After its kernel, a
+ * call copies the status word to device_status_out and clears it, so the next
+ * call starts from zero; calls that overlap on the GPU (different streams, no
+ * ordering between them) race on the word and may see each other's bits.
+ * A rejected call enqueues nothing.
+ */
+qnre_status_t qnre_forward_noalloc(int hidden, int num_heads, int P, qnre_layout_t layout,
+                                   qnre_rope_t rope_style, unsigned flags, int B, int S_local,
+                                   const void* x, const void* w_qkv, const void* q_norm_w,
+                                   const void* k_norm_w, const float* cos_sin, int64_t n_pos,
+                                   const int32_t* positions, const qnre_out_t* out,
+                                   unsigned* device_status_out, qnre_stream_t stream);
+
+/*
  * ulysses_pack_head_chunk -- [PACK]: select local head band
  * [head_offset, head_offset + head_count) inside every destination rank's
  * H/world_size head slice of q, k and v, fusing q|k|v along the last axis:

@@ -1,0 +1,101 @@
+"""The allocation-free forward (qnre_forward_noalloc) against the plan-based qnre_forward.
+
+qnre_forward_noalloc serves callers that cannot call cudaMalloc when they run
+the projection (a memory pool that forbids raw allocations, a runtime that owns
+all device memory, a server that must not allocate once running): it needs no
+plan and keeps its status word in the library's static device scratch.  This
+file is collected last so that a run stopping at the first failure has already
+run every other test; it also passes on its own in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from ulysses_qkv_proj_gb300 import workloads as WL
+from _util import assert_fused_close, to_dev_bf16, to_host_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from ulysses_qkv_proj_gb300 import binding as qb  # noqa: E402
+
+
+def _noalloc():
+    lib = qb.load_library()
+    fn = lib.qnre_forward_noalloc
+    c_int, c_vp = ctypes.c_int, ctypes.c_void_p
+    fn.restype = c_int
+    fn.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.c_uint, c_int, c_int,
+                   c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int64, c_vp, ctypes.POINTER(qb._Out), c_vp, c_vp]
+    return fn
+
+
+def _inputs(wl, bad_positions=()):
+    inp = WL.make_fused_inputs(wl)
+    if bad_positions:
+        inp.positions = inp.positions.copy()
+        flat = inp.positions.reshape(-1)
+        for t in bad_positions:
+            flat[t] = wl.n_pos + 5
+    return dict(x=to_dev_bf16(inp.x), w=to_dev_bf16(inp.w), qw=to_dev_bf16(inp.q_norm_w),
+                kw=to_dev_bf16(inp.k_norm_w), cs=torch.from_numpy(inp.cos_sin).cuda(),
+                pos=torch.from_numpy(inp.positions).cuda())
+
+
+def _call_noalloc(fn, wl, d, out, status):
+    o = qb._Out(*(out[g].data_ptr() if g in out else None for g in ("q", "k", "v", "fused")))
+    return fn(wl.hidden, wl.num_heads, wl.P, qb.LAYOUTS[wl.layout], qb.ROPE_STYLES[wl.rope_style], 0,
+              wl.B, wl.S, d["x"].data_ptr(), d["w"].data_ptr(), d["qw"].data_ptr(), d["kw"].data_ptr(),
+              d["cs"].data_ptr(), d["cs"].shape[0], d["pos"].data_ptr(), ctypes.byref(o), status.data_ptr(),
+              torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_forward_matches_plan_forward_on_two_calls_in_a_row():
+    fn = _noalloc()
+    calls = [
+        # first call: one token with a position outside the table -> its q/k rows are NaN
+        (WL.FusedWorkload("noalloc_a", P=2, B=2, S=200, num_heads=4), (37,)),
+        # second call, straight after: another geometry; its status must not carry the first call's bit
+        (WL.FusedWorkload("noalloc_b", P=4, B=1, S=96, num_heads=8, layout="fused",
+                          rope_style="interleaved"), ()),
+    ]
+    status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    results = []
+    for i, (wl, bad) in enumerate(calls):
+        d = _inputs(wl, bad)
+        plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S,
+                       rope_style=wl.rope_style)
+        ref = qb.alloc_outputs(plan, wl.B, wl.S)
+        qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], ref)
+        out = qb.alloc_outputs(plan, wl.B, wl.S)
+        for t in out.values():
+            t.view(torch.int16).fill_(-1)
+        st = _call_noalloc(fn, wl, d, out, status[i:i + 1])
+        assert st == 0, qb.STATUS_NAMES.get(st, st)
+        torch.cuda.synchronize()
+        plan_bits = plan.device_status()
+        results.append((wl, ref, out, plan_bits))
+    bits = status.cpu().tolist()
+    assert bits[0] == qb.DEVICE_BAD_POSITION and results[0][3] == qb.DEVICE_BAD_POSITION
+    assert bits[1] == 0 and results[1][3] == 0
+    for wl, ref, out, _ in results:
+        for g in ref:
+            assert_fused_close(to_host_f64(out[g]), to_host_f64(ref[g]), what=f"{wl.name}/{g}")
+
+
+def test_noalloc_rejects_before_enqueueing():
+    fn = _noalloc()
+    wl = WL.FusedWorkload("noalloc_c", P=2, B=1, S=64, num_heads=4)
+    d = _inputs(wl)
+    out = {g: torch.empty((2, 1, 128, 2, 128), dtype=torch.bfloat16, device="cuda") for g in "qkv"}
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    o = qb._Out(out["q"].data_ptr(), out["k"].data_ptr(), out["v"].data_ptr(), None)
+    stream = torch.cuda.current_stream().cuda_stream
+    args = [d["x"].data_ptr(), d["w"].data_ptr(), d["qw"].data_ptr(), d["kw"].data_ptr(), d["cs"].data_ptr(),
+            d["cs"].shape[0], d["pos"].data_ptr(), ctypes.byref(o), status.data_ptr(), stream]
+    assert fn(500, 4, 2, 0, 0, 0, 1, 64, *args) == 1             # hidden != heads * 128
+    assert fn(512, 4, 3, 0, 0, 0, 1, 64, *args) == 1             # heads % P != 0
+    assert fn(512, 4, 2, 0, 0, 0, 1 << 20, 1 << 12, *args) == 5  # tokens beyond the kernel's range
+    torch.cuda.synchronize()
+    assert status.item() == 12345                                # nothing was enqueued

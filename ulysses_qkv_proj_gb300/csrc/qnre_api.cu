@@ -432,4 +432,117 @@ qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, in
   return from_cuda(qnre::launch_seg_copy(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// --------------------------------------------------------------------------
+// Allocation-free forward.  Some callers cannot call cudaMalloc at the point
+// where they run the projection: code inside a framework's memory pool that
+// forbids raw device allocations, a runtime that has handed all device memory
+// to its own allocator, or a process that must not allocate once it is
+// serving.  qnre_plan_create allocates the plan's status word with cudaMalloc,
+// so those callers cannot make a plan.  qnre_forward_noalloc needs no plan: its
+// only scratch is the status word, kept in the static device array below, and
+// it makes no device allocation at all.
+// --------------------------------------------------------------------------
+namespace {
+
+// Scratch of the allocation-free forward: every GPU that loads this library
+// holds these 256 bytes until the process exits.  A call uses the first 16
+// (one 4-byte status word, padded like the plan's).
+constexpr size_t kNoAllocScratchBytes = 256;
+constexpr size_t kNoAllocStatusBytes = 16;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+  bool ready = false;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// One-time set-up per device, with that device current: the kernel's
+// shared-memory opt-in and the device address of the static scratch array
+// (the array's name is only a host-side stand-in in host code).
+qnre_status_t noalloc_setup(int dev, NoAllocDevice* out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return QNRE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& st = g_noalloc_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QNRE_ERR_CUDA;
+    if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
+    if (qnre::prepare_fused_qkv_kernel() != cudaSuccess) return QNRE_ERR_CUDA;
+    if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return QNRE_ERR_CUDA;
+    st.scratch = p;
+    st.num_sms = sms;
+    st.ready = true;
+  }
+  *out = st;
+  return QNRE_OK;
+}
+
+}  // namespace
+
+qnre_status_t qnre_forward_noalloc(int hidden, int num_heads, int P, qnre_layout_t layout, qnre_rope_t rope_style,
+                                   unsigned flags, int B, int S_local, const void* x, const void* w_qkv,
+                                   const void* q_norm_w, const void* k_norm_w, const float* cos_sin, int64_t n_pos,
+                                   const int32_t* positions, const qnre_out_t* out, unsigned* device_status_out,
+                                   qnre_stream_t stream) {
+  // The geometry checks of qnre_plan_create, without its allocation.
+  if (num_heads < 1 || P < 1 || hidden < 1) return QNRE_ERR_INVALID_ARG;
+  if (hidden != num_heads * QNRE_HEAD_DIM || hidden % 64 != 0 || num_heads % P != 0) return QNRE_ERR_INVALID_ARG;
+  if (layout != QNRE_LAYOUT_BSHD && layout != QNRE_LAYOUT_FUSED) return QNRE_ERR_INVALID_ARG;
+  if (rope_style != QNRE_ROPE_ROTATE_HALF && rope_style != QNRE_ROPE_INTERLEAVED) return QNRE_ERR_INVALID_ARG;
+  if ((flags & ~QNRE_FLAG_EPILOGUE_OFF) != 0) return QNRE_ERR_INVALID_ARG;
+  if (B < 0 || S_local < 0) return QNRE_ERR_INVALID_ARG;
+  // Sizes beyond what this entry point serves: the status block must fit the
+  // static scratch, and the token count must stay inside the kernel's 32-bit
+  // tile and TMA coordinates (the same bound qnre_plan_create puts on max_tokens).
+  if (kNoAllocStatusBytes > kNoAllocScratchBytes) return QNRE_ERR_CAPACITY;
+  const int64_t tokens_per_rank = static_cast<int64_t>(B) * S_local;
+  if (tokens_per_rank * static_cast<int64_t>(P) > (int64_t{1} << 31) - 256) return QNRE_ERR_CAPACITY;
+  if (device_status_out != nullptr && !aligned(device_status_out, 4)) return QNRE_ERR_ALIGNMENT;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QNRE_ERR_CUDA;
+  NoAllocDevice st;
+  const qnre_status_t s0 = noalloc_setup(dev, &st);
+  if (s0 != QNRE_OK) return s0;
+
+  // A plan on the host stack whose status word is the static scratch.
+  qnre_plan_s plan;
+  plan.hidden = hidden;
+  plan.num_heads = num_heads;
+  plan.P = P;
+  plan.H_local = num_heads / P;
+  plan.layout = layout;
+  plan.max_tokens = tokens_per_rank > 0 ? tokens_per_rank : 1;
+  plan.rope_style = rope_style;
+  plan.flags = flags;
+  plan.device = dev;
+  plan.num_sms = st.num_sms;
+  plan.d_status = static_cast<unsigned*>(st.scratch);
+
+  const qnre_status_t s1 = qnre_forward(&plan, B, S_local, x, w_qkv, q_norm_w, k_norm_w, cos_sin, n_pos, positions,
+                                        out, stream);
+  if (s1 != QNRE_OK) return s1;  // nothing was enqueued
+  if (tokens_per_rank == 0) {
+    if (device_status_out == nullptr) return QNRE_OK;
+    return from_cuda(cudaMemsetAsync(device_status_out, 0, sizeof(unsigned), reinterpret_cast<cudaStream_t>(stream)));
+  }
+  // The kernel ORs bits into the status word, so it must be zero when the next
+  // call's kernel starts: hand this call's word to the caller, then clear it,
+  // both in stream order behind the kernel.
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (device_status_out != nullptr &&
+      cudaMemcpyAsync(device_status_out, st.scratch, sizeof(unsigned), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return QNRE_ERR_CUDA;
+  return from_cuda(cudaMemsetAsync(st.scratch, 0, kNoAllocStatusBytes, s));
+}
+
 }  // extern "C"
