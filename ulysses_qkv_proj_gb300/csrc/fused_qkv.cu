@@ -11,21 +11,24 @@
 //   local head h % H_local, global row r_s * S + s.
 //
 // How (this kernel's design, not the pages'):
-//   * persistent grid, one CTA per SM, tiles of 128 tokens x 256 columns
-//     (= 2 heads) walked in a grouped raster so concurrent CTAs share x and W
-//     panels in L2;
-//   * warp 0: one thread issues TMA loads of x (K-major) and W (N-major) into a
-//     4-stage shared-memory ring (128-byte swizzle);
-//   * warp 1: one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32
-//     accumulate in tensor memory), double-buffering the accumulator so the
-//     epilogue of tile i overlaps the main loop of tile i+1;
-//   * warps 2-5: epilogue; thread i owns TMEM lane i = token row i of the tile,
-//     so a head's 128 values are thread-local: the RMS sum, the scale and both
-//     RoPE pairings need no cross-thread traffic; each thread then writes its
-//     head row (256 contiguous bytes) straight to the band destination.
+//   * persistent grid of CTA pairs (clusters of 2, one CTA per SM); a pair owns
+//     a 256-token x 256-column tile (= 2 heads), tiles walked in a grouped
+//     raster so concurrent pairs share x and W panels in L2;
+//   * warp 0 of each CTA: one thread issues TMA loads of its 128 x-rows
+//     (K-major) and its 128 W-columns (N-major) into a 6-stage ring (128-byte
+//     swizzle); both CTAs' loads complete on the leader CTA's stage barrier;
+//   * warp 1 of the leader: one thread issues tcgen05.mma.cta_group::2 (M=256,
+//     N=256, K=16, bf16 in, fp32 accumulate in each CTA's tensor memory),
+//     double-buffering the accumulator so the epilogue of tile i overlaps the
+//     main loop of tile i+1; commits are multicast to both CTAs;
+//   * warps 2-5 of each CTA: epilogue; thread i owns TMEM lane i = token row i
+//     of that CTA's half, so a head's 128 values are thread-local: the RMS sum,
+//     the scale and both RoPE pairings need no cross-thread traffic; each
+//     thread writes its head row (256 contiguous bytes) straight to the band
+//     destination, then both CTAs release the accumulator on the leader.
 //   * every mbarrier wait has a time limit; on expiry the kernel raises a
-//     status bit, drains its own in-flight copies and MMAs, frees its tensor
-//     memory and returns.
+//     status bit, tells the peer CTA to stop, drains its own in-flight copies
+//     and MMAs, frees its tensor memory and returns.
 #include "fused_qkv.cuh"
 #include "ptx.cuh"
 #include "../../include/qnre.h"
@@ -36,19 +39,28 @@ namespace qnre {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kBN, /*b_mn_major=*/true);
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPairM, kBN, /*b_mn_major=*/true);
+constexpr uint64_t kDrainGraceNs = 50ull * 1000ull;  // in-flight TMA settles in microseconds
 
 struct SmemLayout {
   uint32_t a;      // kStages x kABytes
   uint32_t b;      // kStages x kBBytes
-  uint32_t full;   // kStages mbarriers: TMA -> MMA
-  uint32_t empty;  // kStages mbarriers: MMA -> TMA
-  uint32_t tfull;  // 2 mbarriers: MMA -> epilogue
-  uint32_t tempty; // 2 mbarriers: epilogue -> MMA
-  uint32_t drain;  // 1 mbarrier: MMA completion on abort
+  uint32_t full;   // kStages mbarriers: TMA -> MMA (the leader's count both CTAs' bytes)
+  uint32_t empty;  // kStages mbarriers: MMA -> TMA (both CTAs, multicast commit)
+  uint32_t tfull;  // 2 mbarriers: MMA -> epilogue (both CTAs, multicast commit)
+  uint32_t tempty; // 2 mbarriers: epilogues of both CTAs -> MMA (leader)
+  uint32_t drain;  // 1 mbarrier: MMA completion on abort (leader)
+  uint32_t abort;  // abort word (shared address)
+  uint32_t rank;   // 0 = leader, 1 = peer
 };
 
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
+__device__ __forceinline__ void raise_abort(const SmemLayout& L, volatile uint32_t* abort_flag, unsigned* status) {
+  *abort_flag = 1u;
+  ptx::st_shared_cluster_u32(ptx::mapa_shared(L.abort, L.rank ^ 1u), 1u);
+  atomicOr(status, QNRE_DEVICE_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const SmemLayout& L,
                                              volatile uint32_t* abort_flag, unsigned* status,
                                              bool honour_abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -58,11 +70,16 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
     if ((i & 31u) == 0) {
       if (honour_abort && *abort_flag) return false;
       if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(status, QNRE_DEVICE_WAIT_TIMEOUT);
+        if (honour_abort) raise_abort(L, abort_flag, status);
         return false;
       }
     }
+  }
+}
+
+__device__ __forceinline__ void grace_spin(uint64_t ns) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (ptx::global_timer_ns() - t0 < ns) {
   }
 }
 
@@ -105,57 +122,71 @@ __device__ __forceinline__ void rotate(float& a, float& b, float c, float s) {
 }
 
 // --------------------------------------------------------------------------
-// Producer: TMA loads of the x and W tiles into the stage ring.
+// Producer (both CTAs): TMA loads of this CTA's x rows and W columns.
 // --------------------------------------------------------------------------
 __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile uint32_t* abort_flag) {
   uint32_t g = 0;
   uint32_t used_mask = 0, parity_mask = 0;  // per stage: ever loaded / parity of its last load
+  const uint64_t pol_x = ptx::l2_policy_evict_last();
   const uint64_t pol_w = ptx::l2_policy_evict_last();
+  const uint32_t full_leader = ptx::mapa_shared(L.full, 0);
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+  for (int tile = pair; ok && tile < a.num_tiles; tile += num_pairs) {
     int m_blk, n_blk;
     tile_coords(tile, a, m_blk, n_blk);
+    const int row0 = m_blk * kPairM + static_cast<int>(L.rank) * kBM;
+    const int col0 = n_blk * kBN + static_cast<int>(L.rank) * kBNHalf;
     for (int kb = 0; kb < a.num_k_blocks; ++kb, ++g) {
       const uint32_t s = g % kStages;
       const uint32_t ph = (g / kStages) & 1u;
-      if (!bounded_wait(L.empty + 8 * s, ph ^ 1u, abort_flag, a.status, true)) {
+      if (!bounded_wait(L.empty + 8 * s, ph ^ 1u, L, abort_flag, a.status, true)) {
         ok = false;
         break;
       }
-      const uint32_t full = L.full + 8 * s;
-      ptx::mbar_arrive_expect_tx(full, kABytes + kBBytes);
-      ptx::tma_load_2d(L.a + s * kABytes, &a.tmap_x, full, kb * kBK, m_blk * kBM);
+      if (L.rank == 0) ptx::mbar_arrive_expect_tx(L.full + 8 * s, 2 * kStageBytes);
+      const uint32_t bar = full_leader + 8 * s;
+      ptx::tma_load_2d_pair(L.a + s * kABytes, &a.tmap_x, bar, kb * kBK, row0, pol_x);
 #pragma unroll
-      for (int j = 0; j < kBN / 64; ++j) {
-        ptx::tma_load_2d_hint(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, full,
-                              n_blk * kBN + j * 64, kb * kBK, pol_w);
+      for (int j = 0; j < kBNHalf / 64; ++j) {
+        ptx::tma_load_2d_pair(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, bar, col0 + j * 64, kb * kBK,
+                              pol_w);
       }
       used_mask |= 1u << s;
       parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
     }
   }
   if (!ok) {
-    // Abort: let every load already issued land before the CTA can exit.
-    for (uint32_t s = 0; s < kStages; ++s) {
-      if (used_mask & (1u << s)) {
-        bounded_wait(L.full + 8 * s, (parity_mask >> s) & 1u, abort_flag, a.status, false);
+    // Abort: let every load already issued land before the CTA can exit.  The
+    // leader's stage barriers count both CTAs' bytes; the peer cannot observe
+    // its own loads, so both also wait a short grace period.
+    if (L.rank == 0) {
+      for (uint32_t s = 0; s < kStages; ++s) {
+        if (used_mask & (1u << s)) {
+          bounded_wait(L.full + 8 * s, (parity_mask >> s) & 1u, L, abort_flag, a.status, false);
+        }
       }
     }
+    grace_spin(kDrainGraceNs);
   }
 }
 
 // --------------------------------------------------------------------------
-// MMA issuer: tcgen05.mma over the stage ring into the TMEM accumulators.
+// MMA issuer (leader CTA only): tcgen05.mma over the stage ring into the TMEM
+// accumulators of both CTAs.
 // --------------------------------------------------------------------------
 __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
                         volatile uint32_t* abort_flag) {
   uint32_t g = 0;
   uint32_t it = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++it) {
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  for (int tile = pair; ok && tile < a.num_tiles; tile += num_pairs, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
-    if (!bounded_wait(L.tempty + 8 * acc, aph ^ 1u, abort_flag, a.status, true)) {
+    if (!bounded_wait(L.tempty + 8 * acc, aph ^ 1u, L, abort_flag, a.status, true)) {
       ok = false;
       break;
     }
@@ -164,7 +195,7 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
     for (int kb = 0; kb < a.num_k_blocks; ++kb, ++g) {
       const uint32_t s = g % kStages;
       const uint32_t ph = (g / kStages) & 1u;
-      if (!bounded_wait(L.full + 8 * s, ph, abort_flag, a.status, true)) {
+      if (!bounded_wait(L.full + 8 * s, ph, L, abort_flag, a.status, true)) {
         ok = false;
         break;
       }
@@ -179,16 +210,16 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
         // B: N-major, 64-column blocks of kBK rows x 128 B (LBO = 8 KiB apart),
         //    8-row k groups 1024 B apart; the k-th 16-row slice starts 2 KiB in.
         const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024);
-        ptx::umma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        ptx::umma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      ptx::umma_commit(L.empty + 8 * s);  // frees the stage once these MMAs finish
+      ptx::umma_commit_pair_multicast(L.empty + 8 * s, 0x3);  // frees the stage in both CTAs
     }
     if (!ok) break;
-    ptx::umma_commit(L.tfull + 8 * acc);  // accumulator ready for the epilogue
+    ptx::umma_commit_pair_multicast(L.tfull + 8 * acc, 0x3);  // accumulators ready in both CTAs
   }
   if (!ok) {
-    ptx::umma_commit(L.drain);
-    bounded_wait(L.drain, 0, abort_flag, a.status, false);
+    ptx::umma_commit_pair(L.drain);
+    bounded_wait(L.drain, 0, L, abort_flag, a.status, false);
   }
 }
 
@@ -203,16 +234,19 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   const int row = sub * 32 + lane;
   const int S_g = a.P * a.S;
   const int three_h = 3 * a.H;
+  const uint32_t tempty_leader = ptx::mapa_shared(L.tempty, 0);
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
   uint32_t it = 0;
-  for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++it) {
+  for (int tile = pair; tile < a.num_tiles; tile += num_pairs, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
-    if (!bounded_wait(L.tfull + 8 * acc, aph, abort_flag, a.status, true)) break;
+    if (!bounded_wait(L.tfull + 8 * acc, aph, L, abort_flag, a.status, true)) break;
     ptx::tc_fence_after_sync();
 
     int m_blk, n_blk;
     tile_coords(tile, a, m_blk, n_blk);
-    const int t = m_blk * kBM + row;
+    const int t = m_blk * kPairM + static_cast<int>(L.rank) * kBM + row;
     const bool valid = t < a.T;
     const int s_loc = valid ? t % a.S : 0;
     const int tb = valid ? t / a.S : 0;
@@ -356,10 +390,10 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
     }
     if (bad_pos && valid) atomicOr(a.status, QNRE_DEVICE_BAD_POSITION);
 
-    // Hand the accumulator back to the MMA warp.
+    // Hand the accumulator back to the leader's MMA thread.
     ptx::tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(L.tempty + 8 * acc);
+    if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader + 8 * acc);
   }
 }
 
@@ -378,9 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   L.tfull = L.empty + 8 * kStages;
   L.tempty = L.tfull + 16;
   L.drain = L.tempty + 16;
-  uint8_t* bar_ptr = smem + kStages * (kABytes + kBBytes);
+  uint8_t* bar_ptr = smem + kStages * kStageBytes;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kStages + 5));
   volatile uint32_t* abort_flag = tmem_holder + 1;
+  L.abort = ptx::smem_addr(tmem_holder + 1);
+  L.rank = ptx::cluster_ctarank();
   float* norm_w = reinterpret_cast<float*>(bar_ptr + kBarBytes);
 
   const int warp = threadIdx.x / 32;
@@ -390,20 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
     ptx::prefetch_tensormap(&args.tmap_x);
     ptx::prefetch_tensormap(&args.tmap_w);
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(L.full + 8 * s, 1);
-      ptx::mbar_init(L.empty + 8 * s, 1);
+      ptx::mbar_init(L.full + 8 * s, 1);   // the leader's expect_tx arrival
+      ptx::mbar_init(L.empty + 8 * s, 1);  // one multicast commit
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(L.tfull + 8 * i, 1);
-      ptx::mbar_init(L.tempty + 8 * i, 4);  // one arrival per epilogue warp
+      ptx::mbar_init(L.tfull + 8 * i, 1);   // one multicast commit
+      ptx::mbar_init(L.tempty + 8 * i, 8);  // four epilogue warps in each CTA
     }
     ptx::mbar_init(L.drain, 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
-    ptx::tmem_relinquish_alloc_permit();
+    ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   if (threadIdx.x >= 64) {
     const int d = threadIdx.x - 64;  // 0..127
@@ -412,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any remote use
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -419,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
     if (lane == 0) run_producer(args, L, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma(args, L, tmem_base, abort_flag);
+    if (lane == 0 && L.rank == 0) run_mma(args, L, tmem_base, abort_flag);
     __syncwarp();
   } else {
     run_epilogue(args, L, tmem_base, norm_w, abort_flag);
@@ -427,21 +464,53 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
 
   ptx::tc_fence_before_sync();
   __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still signal it or use its memory
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
 }  // namespace
 
-cudaError_t prepare_fused_qkv_kernel() {
-  return cudaFuncSetAttribute(fused_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+cudaError_t prepare_fused_qkv_kernel(int* max_pairs) {
+  cudaError_t e = cudaFuncSetAttribute(fused_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&clusters, fused_qkv_kernel, &cfg)) != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  *max_pairs = clusters;
+  return cudaSuccess;
 }
 
-cudaError_t launch_fused_qkv(const FusedArgs& args, int grid, cudaStream_t stream) {
-  fused_qkv_kernel<<<grid, kThreads, kSmemBytes, stream>>>(args);
-  return cudaGetLastError();
+cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_qkv_kernel, args);
 }
 
 }  // namespace qnre

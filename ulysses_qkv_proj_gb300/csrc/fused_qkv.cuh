@@ -8,19 +8,25 @@
 
 namespace qnre {
 
-// Tile geometry.  One CTA owns a BM x BN tile of Y = x W: BM tokens by two
-// 128-wide heads, so the whole head row of a token is one TMEM lane.
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+// Tile geometry.  A cluster of two CTAs (an SM pair) owns a 256 x 256 tile of
+// Y = x W: 256 tokens by two 128-wide heads.  Each CTA holds 128 of the rows
+// (its own A half and its own accumulator rows) and 128 of the columns of the
+// B tile; the pair's tcgen05.mma (cta_group::2) combines them.  A token's whole
+// head row is one TMEM lane of one CTA.
+constexpr int kBM = 128;                      // rows per CTA (256 per pair)
+constexpr int kPairM = 2 * kBM;
+constexpr int kBN = 256;                      // columns per tile (two heads)
+constexpr int kBNHalf = kBN / 2;              // B columns held by each CTA
 constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kABytes = kBM * kBK * 2;        // 16 KiB
-constexpr int kBBytes = kBN * kBK * 2;        // 32 KiB
+constexpr int kBBytes = kBNHalf * kBK * 2;    // 16 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = kBN;                 // fp32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator
 constexpr int kBarBytes = 256;                // mbarriers + small words
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kABytes + kBBytes) + kBarBytes +
+constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
                            2 * 128 * 4 /*norm weights*/;
 
 struct FusedArgs {
@@ -40,13 +46,14 @@ struct FusedArgs {
   int layout;       // 0 bshd, 1 fused
   int rope_style;   // 0 rotate-half, 1 interleaved
   int epilogue_on;  // 0: bare projection
-  int num_m_tiles, num_n_tiles, num_tiles, group_m, num_k_blocks;
+  int num_m_tiles, num_n_tiles, num_tiles, group_m, num_k_blocks;  // m tiles are 256 rows
 };
 
-// Enqueue the fused kernel.  `grid` CTAs walk the tile list persistently.
-cudaError_t launch_fused_qkv(const FusedArgs& args, int grid, cudaStream_t stream);
+// Enqueue the fused kernel: `pairs` CTA pairs walk the tile list persistently.
+cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream);
 
-// One-time per-device kernel attribute setup (shared-memory opt-in).
-cudaError_t prepare_fused_qkv_kernel();
+// One-time per-device kernel setup (shared-memory opt-in); returns in
+// *max_pairs how many CTA pairs of this kernel fit on the current device at once.
+cudaError_t prepare_fused_qkv_kernel(int* max_pairs);
 
 }  // namespace qnre

@@ -23,7 +23,7 @@ struct qnre_plan_s {
   qnre_rope_t rope_style = QNRE_ROPE_ROTATE_HALF;
   unsigned flags = 0;
   int device = -1;
-  int num_sms = 0;
+  int max_pairs = 0;  // CTA pairs of the fused kernel resident at once
   unsigned* d_status = nullptr;
 };
 
@@ -157,13 +157,12 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return QNRE_ERR_CUDA;
-  int major = 0, minor = 0, sms = 0;
+  int major = 0, minor = 0, pairs = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return QNRE_ERR_CUDA;
   if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
-  if (qnre::prepare_fused_qkv_kernel() != cudaSuccess) return QNRE_ERR_CUDA;
+  if (qnre::prepare_fused_qkv_kernel(&pairs) != cudaSuccess) return QNRE_ERR_CUDA;
   if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
 
   qnre_plan_s* p = new (std::nothrow) qnre_plan_s();
@@ -186,7 +185,7 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
   p->rope_style = rope_style;
   p->flags = flags;
   p->device = dev;
-  p->num_sms = sms;
+  p->max_pairs = pairs;
   *plan = p;
   return QNRE_OK;
 }
@@ -277,16 +276,20 @@ qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.layout = bshd ? 0 : 1;
   a.rope_style = plan->rope_style == QNRE_ROPE_INTERLEAVED ? 1 : 0;
   a.epilogue_on = (plan->flags & QNRE_FLAG_EPILOGUE_OFF) ? 0 : 1;
-  const int64_t m_tiles = (T + qnre::kBM - 1) / qnre::kBM;
+  const int64_t m_tiles = (T + qnre::kPairM - 1) / qnre::kPairM;
   const int64_t n_tiles = (N + qnre::kBN - 1) / qnre::kBN;
   if (m_tiles * n_tiles > INT32_MAX) return QNRE_ERR_CAPACITY;
   a.num_m_tiles = static_cast<int>(m_tiles);
   a.num_n_tiles = static_cast<int>(n_tiles);
   a.num_tiles = a.num_m_tiles * a.num_n_tiles;
-  a.group_m = std::min(a.num_m_tiles, 16);
+  // Raster: groups of group_m row tiles sweep every column tile, rows fastest.
+  // The group's x panels (256 rows x hidden each) stay resident in L2 while W
+  // streams past; keep them to about 48 MB of the 129 MB L2.
+  const int64_t panel_bytes = static_cast<int64_t>(qnre::kPairM) * K * 2;
+  a.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(m_tiles, (48ll << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
-  const int grid = std::min(a.num_tiles, plan->num_sms);
-  return from_cuda(qnre::launch_fused_qkv(a, grid, reinterpret_cast<cudaStream_t>(stream)));
+  const int pairs = std::min(a.num_tiles, plan->max_pairs);
+  return from_cuda(qnre::launch_fused_qkv(a, pairs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, unsigned* bits, int clear) {
@@ -455,7 +458,7 @@ constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
   bool ready = false;
   void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  int num_sms = 0;
+  int max_pairs = 0;
 };
 std::mutex g_noalloc_mu;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
@@ -468,18 +471,17 @@ qnre_status_t noalloc_setup(int dev, NoAllocDevice* out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   NoAllocDevice& st = g_noalloc_dev[dev];
   if (!st.ready) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, pairs = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return QNRE_ERR_CUDA;
     if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
-    if (qnre::prepare_fused_qkv_kernel() != cudaSuccess) return QNRE_ERR_CUDA;
+    if (qnre::prepare_fused_qkv_kernel(&pairs) != cudaSuccess) return QNRE_ERR_CUDA;
     if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return QNRE_ERR_CUDA;
     st.scratch = p;
-    st.num_sms = sms;
+    st.max_pairs = pairs;
     st.ready = true;
   }
   *out = st;
@@ -525,7 +527,7 @@ qnre_status_t qnre_forward_noalloc(int hidden, int num_heads, int P, qnre_layout
   plan.rope_style = rope_style;
   plan.flags = flags;
   plan.device = dev;
-  plan.num_sms = st.num_sms;
+  plan.max_pairs = st.max_pairs;
   plan.d_status = static_cast<unsigned*>(st.scratch);
 
   const qnre_status_t s1 = qnre_forward(&plan, B, S_local, x, w_qkv, q_norm_w, k_norm_w, cos_sin, n_pos, positions,
