@@ -42,6 +42,38 @@ SCHEDULE = WL.BENCH_SCHEDULE
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+FUSED_SOURCES = ["ulysses_qkv_proj_gb300/csrc/fused_qkv.cu", "ulysses_qkv_proj_gb300/csrc/fused_qkv.cuh",
+                 "ulysses_qkv_proj_gb300/csrc/ptx.cuh"]
+FUSED_PROFILE = "profiles/fused_qkv_kernel_h4096_p4_s4096.md"
+
+
+def fused_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, FUSED_PROFILE)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel-source-hash") != fused_source_hash():
+        return None
+    try:
+        return int(fields["traffic-bytes-per-launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,7 +292,7 @@ def run_gpu(args):
                        "schedule": [list(b) for b in SCHEDULE], "l2": "flushed (512 MB write) between steps",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                         "frac": round(tflops / tc_peak, 4), "traffic": None,
+                         "frac": round(tflops / tc_peak, 4), "traffic": profiled_traffic(),
                          "kernel": "fused_qkv_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "flops_per_launch": flops},
             "fused": {"ms": round(fused_avg, 5), "tflops": round(tflops, 1), "tokens_per_s": round(wl.T / (fused_avg * 1e-3), 1)},
@@ -387,6 +419,109 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_workload(args):
+    """One row of the hot path alone on a named workload (not the headline step):
+    the fused op on a FUSED_WORKLOADS shape, or pack + merge over a HEADCHUNK_WORKLOADS shape."""
+    import torch
+
+    from ulysses_qkv_proj_gb300 import binding as qb
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+
+    def t16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+            flush.zero_()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        clocks = ClockSampler(0)
+        clocks.start()
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+            flush.zero_()
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs), clocks.stop()
+
+    name = args.workload
+    if name in WL.FUSED_WORKLOADS:
+        wl = WL.FUSED_WORKLOADS[name]
+        inp = WL.make_fused_inputs(wl)
+        x, w = t16(inp.x), t16(inp.w)
+        qw, kw = t16(inp.q_norm_w), t16(inp.k_norm_w)
+        cs = torch.from_numpy(inp.cos_sin).to(dev)
+        pos = torch.from_numpy(inp.positions).to(dev)
+        plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
+        out = qb.alloc_outputs(plan, wl.B, wl.S, dev)
+        ms, clk = timed(lambda: qb.qnre_forward(plan, x, w, qw, kw, cs, pos, out))
+        if plan.device_status() != 0:
+            raise RuntimeError("device status raised")
+        tflops = wl.flops() / (ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        line = {"metric": "fused QKV+norm+RoPE+scatter tokens/s", "value": round(wl.T / (ms * 1e-3), 1),
+                "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms, 5), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": name, "tokens": wl.T, "hidden": wl.hidden, "layout": wl.layout,
+                           "l2": "flushed between launches"},
+                "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tflops / peak, 4), "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                "gpu_launches": args.steps, "clocks": clk}
+        plan.destroy()
+    elif name in WL.HEADCHUNK_WORKLOADS:
+        wl = WL.HEADCHUNK_WORKLOADS[name]
+        buf = t16(WL.make_headchunk_buffer(wl.B, wl.S_global, wl.num_heads, wl.D))
+        W, L, D, S = wl.P, wl.H_local, wl.D, wl.S
+        views = [(buf[:, r * S:(r + 1) * S, 0], buf[:, r * S:(r + 1) * S, 1], buf[:, r * S:(r + 1) * S, 2])
+                 for r in range(wl.P)]
+        packed = [[torch.empty((wl.B, S, W * cnt, 3 * D), dtype=torch.bfloat16, device=dev) for _, cnt in wl.schedule]
+                  for _ in range(wl.P)]
+        merged = [torch.empty((wl.B, S, wl.num_heads, D), dtype=torch.bfloat16, device=dev) for _ in range(wl.P)]
+
+        def pack_all():
+            for r, (q, k, v) in enumerate(views):
+                for i, (off, cnt) in enumerate(wl.schedule):
+                    qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, packed[r][i])
+
+        def merge_all():
+            for r in range(wl.P):
+                for i, (off, cnt) in enumerate(wl.schedule):
+                    qb.ulysses_merge_output_head_chunk(packed[r][i][..., :D], W, L, off, merged[r])
+
+        ms_p, clk = timed(pack_all)
+        ms_m, _ = timed(merge_all)
+        for r in range(wl.P):
+            if not torch.equal(merged[r], views[r][0]):
+                raise RuntimeError("pack -> merge did not reproduce q")
+        elt = 2
+        pack_bytes = sum(2 * wl.B * S * W * cnt * 3 * D * elt for _, cnt in wl.schedule) * wl.P
+        merge_bytes = sum(2 * wl.B * S * W * cnt * D * elt for _, cnt in wl.schedule) * wl.P
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        gp, gm = pack_bytes / (ms_p * 1e-3) / 1e9, merge_bytes / (ms_m * 1e-3) / 1e9
+        launches = wl.P * len(wl.schedule)
+        line = {"metric": "head-chunk pack/merge GB/s", "value": round(gp, 1), "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_p + ms_m, 5),
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": name, "schedule": [list(b) for b in wl.schedule], "P": wl.P,
+                           "l2": "flushed between steps"},
+                "roofline": {"bound": "hbm", "achieved": round(gp, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(gp / hbm, 4), "peak_source": f"{peak_src} hbm_gbs"},
+                "pack": {"ms": round(ms_p, 5), "bytes": pack_bytes, "GB/s": round(gp, 1), "frac_hbm": round(gp / hbm, 4),
+                         "launches": launches},
+                "merge": {"ms": round(ms_m, 5), "bytes": merge_bytes, "GB/s": round(gm, 1),
+                          "frac_hbm": round(gm / hbm, 4), "launches": launches},
+                "gpu_launches": 2 * launches * args.steps, "clocks": clk}
+    else:
+        raise SystemExit(f"unknown workload {name!r}")
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,11 +530,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--workload", default=None,
+                    help="time one row alone on this workload instead of the headline step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload:
+        run_gpu_workload(args)
     else:
         run_gpu(args)
 
