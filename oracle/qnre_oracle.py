@@ -25,6 +25,13 @@ Sources, by page and section:
 [PACK]   same API reference, "Head-Chunk Layout and Transport Primitives",
          pack_ulysses_qkv_head_chunk.
 [MERGE]  same section, merge_ulysses_output_head_chunk.
+[XCHG]   same API reference, UlyssesCommunicator.scatter_qkv_head_chunk (pack +
+         one all-to-all; its result is [B, S_global, head_count, 3*D]) and
+         gather_output_head_chunk (x [B, S_global, head_count, D]; the NCCL
+         path packs the sequence split into staging, exchanges, and merges the
+         received band into out [B, S_global/world_size, world_size*local_heads,
+         D]); exchange_chunks: chunk r goes to peer r and lands in slot `rank`
+         there ("Ulysses Context-Parallel All-to-All").
 
 Readings taken where the pages leave a step open (each is listed with its
 reason in the design notes):
@@ -52,7 +59,8 @@ __all__ = [
     "rms_norm", "rope_rotate_half", "rope_interleaved", "apply_rope",
     "project_norm_rope", "token_coords", "band_destination", "place_bands",
     "qnre_forward", "pack_head_chunk", "merge_output_head_chunk",
-    "scatter_heads", "gather_heads", "bf16_ulp", "fused_tolerance",
+    "scatter_heads", "gather_heads", "all_to_all", "pack_output_sequence_chunk",
+    "gather_output_head_chunk", "scatter_qkv_head_chunk", "bf16_ulp", "fused_tolerance",
 ]
 
 
@@ -321,6 +329,65 @@ def gather_heads(y: np.ndarray) -> np.ndarray:
         for r in range(P):
             out[r_s, :, :, r * H_local:(r + 1) * H_local] = y[r, :, r_s * S:(r_s + 1) * S]
     return out
+
+
+# ---------------------------------------------------------------------------
+# The exchange and the head-chunk compositions over P virtual ranks   [XCHG]
+# ---------------------------------------------------------------------------
+def all_to_all(sent):
+    """sent[r][r2] is the chunk rank r sends to rank r2; returns received with
+    received[r2][r] = sent[r][r2] (chunk from rank r lands in slot r on rank r2)."""
+    P = len(sent)
+    return [[sent[r][r2] for r in range(P)] for r2 in range(P)]
+
+
+def pack_output_sequence_chunk(x: np.ndarray, world_size: int) -> np.ndarray:
+    """Sequence split of an output band for the output exchange:
+    x [B, S_global, head_count, D] -> [world_size, B, S_global/world_size, head_count, D],
+    chunk r = sequence rows [r*S_local, (r+1)*S_local) (the rows rank r owns)."""
+    B, S_g, cnt, D = x.shape
+    if world_size < 1 or S_g % world_size:
+        raise ValueError("S_global must be divisible by world_size")
+    S = S_g // world_size
+    out = np.empty((world_size, B, S, cnt, D), dtype=x.dtype)
+    for r in range(world_size):
+        out[r] = x[:, r * S:(r + 1) * S]
+    return out
+
+
+def gather_output_head_chunk(x_ranks: Sequence[np.ndarray], local_heads: int, head_offset: int,
+                             out_ranks: Sequence[np.ndarray]):
+    """One output band on every virtual rank: x_ranks[r] [B, S_global, head_count, D]
+    -> copies of out_ranks[r2] [B, S_local, P*local_heads, D] with the band merged.
+
+    Written as the pages' three steps: sequence-split pack on every rank, the
+    all-to-all, and merge of the received band on every rank."""
+    P = len(x_ranks)
+    staged = [pack_output_sequence_chunk(x, P) for x in x_ranks]
+    received = all_to_all([[staged[r][r2] for r2 in range(P)] for r in range(P)])
+    res = []
+    for r2 in range(P):
+        band = np.stack(received[r2], axis=0)            # [P(src), B, S, cnt, D]
+        P_, B, S, cnt, D = band.shape
+        rec = band.transpose(1, 2, 0, 3, 4).reshape(B, S, P * cnt, D)  # slot = src*cnt + j
+        res.append(merge_output_head_chunk(rec, P, local_heads, head_offset, out_ranks[r2]))
+    return res
+
+
+def scatter_qkv_head_chunk(q_ranks, k_ranks, v_ranks, head_offset: int, head_count: int):
+    """One input band on every virtual rank: q/k/v_ranks[r] [B, S_local, H, D]
+    -> per rank r2 the exchanged payload [B, S_global, head_count, 3*D].
+
+    The pages' steps: pack on every rank, then the all-to-all of the packed
+    payload's destination slots (slots [r2*head_count, (r2+1)*head_count) go to
+    rank r2, which stacks them in source-rank order along the sequence)."""
+    P = len(q_ranks)
+    packed = [pack_head_chunk(q_ranks[r], k_ranks[r], v_ranks[r], P, head_offset, head_count)
+              for r in range(P)]
+    sent = [[packed[r][:, :, r2 * head_count:(r2 + 1) * head_count, :] for r2 in range(P)]
+            for r in range(P)]
+    received = all_to_all(sent)
+    return [np.concatenate(received[r2], axis=1) for r2 in range(P)]
 
 
 # ---------------------------------------------------------------------------

@@ -376,6 +376,46 @@ def check_pack_merge_schedules(golden_dir):
             assert np.array_equal(outs[c], X)
 
 
+def check_sequence_chunk_golden(golden_dir):
+    g = _load(golden_dir, "seqchunk_w2_s4.json")
+    B, S_g, cnt, D, W = g["B"], g["S_global"], g["head_count"], g["D"], g["world_size"]
+    b, s, j, d = np.meshgrid(np.arange(B), np.arange(S_g), np.arange(cnt), np.arange(D), indexing="ij")
+    x = 100 * s + 10 * j + d
+    assert Q.pack_output_sequence_chunk(x, W).tolist() == g["expected"]
+
+
+def check_all_to_all():
+    sent = [[(r, r2) for r2 in range(3)] for r in range(3)]
+    rec = Q.all_to_all(sent)
+    for r2 in range(3):
+        assert rec[r2] == [(r, r2) for r in range(3)]  # slot r on rank r2 holds rank r's chunk for r2
+
+
+def check_head_chunk_exchanges_reconstruct_ordinary(golden_dir):
+    """Every band of a complete schedule through the head-chunk exchanges rebuilds the
+    ordinary scatter_heads / gather_heads results (the pages' reconstruction statements)."""
+    g = _load(golden_dir, "schedules.json")
+    rng = np.random.default_rng(23)
+    for sch in g["schedules"][:2]:
+        L = sch["local_heads"]
+        P, B, S, D = 2, 2, 3, 4
+        H = P * L
+        q, k, v = (rng.integers(0, 1 << 16, size=(P, B, S, H, D)).astype(np.uint16) for _ in range(3))
+        full = {c: Q.scatter_heads(X) for c, X in zip("qkv", (q, k, v))}   # [P, B, P*S, L, D]
+        for off, cnt in sch["bands"]:
+            res = Q.scatter_qkv_head_chunk(list(q), list(k), list(v), off, cnt)
+            for r2 in range(P):
+                assert res[r2].shape == (B, P * S, cnt, 3 * D)
+                for ci, c in enumerate("qkv"):
+                    assert np.array_equal(res[r2][..., ci * D:(ci + 1) * D], full[c][r2][:, :, off:off + cnt])
+        # output side: attention output bands [P, B, P*S, L, D] back to [P, B, S, H, D]
+        o = rng.integers(0, 1 << 16, size=(P, B, P * S, L, D)).astype(np.uint16)
+        outs = [np.zeros((B, S, H, D), np.uint16) for _ in range(P)]
+        for off, cnt in sch["bands"]:
+            outs = Q.gather_output_head_chunk([o[r][:, :, off:off + cnt] for r in range(P)], L, off, outs)
+        assert np.array_equal(np.stack(outs), Q.gather_heads(o))
+
+
 def check_tolerance_rule():
     assert Q.bf16_ulp(np.array([1.0, 1.5, 3.0, -0.25]))[:].tolist() == [2 ** -7, 2 ** -7, 2 ** -6, 2 ** -9]
     tol = Q.fused_tolerance(np.array([0.5, 4.0, 100.0]))
@@ -392,8 +432,10 @@ PLAIN_CHECKS = [
     check_rope_rotate_half_unit_vectors, check_rope_interleaved_unit_vectors,
     check_rope_norm_and_composition, check_rope_table, check_placement_p1_and_coverage,
     check_placement_matches_scatter_heads, check_scatter_gather, check_tolerance_rule,
+    check_all_to_all,
 ]
-GOLDEN_CHECKS = [check_placement_golden, check_pack_golden, check_merge_golden, check_pack_merge_schedules]
+GOLDEN_CHECKS = [check_placement_golden, check_pack_golden, check_merge_golden, check_pack_merge_schedules,
+                 check_sequence_chunk_golden, check_head_chunk_exchanges_reconstruct_ordinary]
 
 
 @pytest.mark.parametrize("check", PLAIN_CHECKS, ids=lambda f: f.__name__)
@@ -504,6 +546,29 @@ def _mut_bf16_decode(bits):
     return (b.astype(np.uint32) << 15).view(np.float32).astype(np.float64)
 
 
+def _mut_seqchunk_wrong_rows(x, world_size):
+    B, S_g, cnt, D = x.shape
+    S = S_g // world_size
+    out = np.empty((world_size, B, S, cnt, D), dtype=x.dtype)
+    for r in range(world_size):
+        out[r] = x[:, r::world_size][:, :S]
+    return out
+
+
+def _mut_all_to_all_identity(sent):
+    return [list(row) for row in sent]
+
+
+def _mut_scatter_heads_swapped(x):
+    P, B, S, H, D = x.shape
+    H_local = H // P
+    out = np.empty((P, B, P * S, H_local, D), dtype=x.dtype)
+    for r in range(P):
+        for r_s in range(P):
+            out[r, :, r_s * S:(r_s + 1) * S] = x[r, :, :, r_s * H_local:(r_s + 1) * H_local]
+    return out
+
+
 MUTANTS = [
     ("qkv_projection", _mut_projection_transposed),
     ("rms_norm", _mut_rms_no_eps),
@@ -518,6 +583,9 @@ MUTANTS = [
     ("merge_output_head_chunk", _mut_merge_wrong_slot),
     ("split_qkv_heads", _mut_split_heads_swapped),
     ("bf16_to_f64", _mut_bf16_decode),
+    ("pack_output_sequence_chunk", _mut_seqchunk_wrong_rows),
+    ("all_to_all", _mut_all_to_all_identity),
+    ("scatter_heads", _mut_scatter_heads_swapped),
 ]
 
 
