@@ -499,6 +499,47 @@ def run_gpu_workload(args):
         for r in range(wl.P):
             if not torch.equal(merged[r], views[r][0]):
                 raise RuntimeError("pack -> merge did not reproduce q")
+
+        # ordinary and composed exchanges over the same P virtual ranks
+        P = wl.P
+        ranks = buf.view(P, S, 3, wl.num_heads, D)                 # [P*B, S, 3, H, D] with B = 1
+        q5 = ranks[:, :, 0].contiguous().view(P, 1, S, wl.num_heads, D)
+        y5 = torch.empty((P, 1, P * S, L, D), dtype=torch.bfloat16, device=dev)
+        g5 = torch.empty_like(q5)
+        pays = [torch.empty((P, 1, P * S, cnt, 3 * D), dtype=torch.bfloat16, device=dev) for _, cnt in wl.schedule]
+        outs = torch.empty_like(q5)
+        seq = [torch.empty((P, 1, S, cnt, D), dtype=torch.bfloat16, device=dev) for _, cnt in wl.schedule]
+        ms_sc, _ = timed(lambda: qb.ulysses_scatter_heads(q5, y5))
+        ms_ga, _ = timed(lambda: qb.ulysses_gather_heads(y5, g5))
+        bands = [y5[:, :, :, off:off + cnt].contiguous() for off, cnt in wl.schedule]  # after y5 is filled
+
+        def sqkv():
+            for i, (off, cnt) in enumerate(wl.schedule):
+                qb.ulysses_scatter_qkv_head_chunk(ranks[:, :, 0], ranks[:, :, 1], ranks[:, :, 2], P, off, cnt, pays[i])
+
+        def gout():
+            for i, (off, cnt) in enumerate(wl.schedule):
+                qb.ulysses_gather_output_head_chunk(bands[i], L, off, outs)
+
+        def seqp():
+            for i, (off, cnt) in enumerate(wl.schedule):
+                qb.ulysses_pack_output_sequence_chunk(bands[i][0], P, seq[i])
+
+        ms_sq, _ = timed(sqkv)
+        ms_go, _ = timed(gout)
+        ms_sp, _ = timed(seqp)
+        if not (torch.equal(g5, q5) and torch.equal(outs, q5)):
+            raise RuntimeError("scatter -> gather did not reproduce q")
+        qbytes = 2 * q5.numel() * 2
+
+        def row(ms, nbytes, launches):
+            g = nbytes / (ms * 1e-3) / 1e9
+            return {"ms": round(ms, 5), "bytes": nbytes, "GB/s": round(g, 1), "frac_hbm": round(g / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), 4),
+                    "launches": launches}
+        extra = {"scatter_heads": row(ms_sc, qbytes, 1), "gather_heads": row(ms_ga, qbytes, 1),
+                 "scatter_qkv_head_chunk": row(ms_sq, 3 * qbytes, len(wl.schedule)),
+                 "gather_output_head_chunk": row(ms_go, qbytes, len(wl.schedule)),
+                 "pack_output_sequence_chunk": row(ms_sp, qbytes // P, len(wl.schedule))}
         elt = 2
         pack_bytes = sum(2 * wl.B * S * W * cnt * 3 * D * elt for _, cnt in wl.schedule) * wl.P
         merge_bytes = sum(2 * wl.B * S * W * cnt * D * elt for _, cnt in wl.schedule) * wl.P
@@ -517,6 +558,7 @@ def run_gpu_workload(args):
                 "merge": {"ms": round(ms_m, 5), "bytes": merge_bytes, "GB/s": round(gm, 1),
                           "frac_hbm": round(gm / hbm, 4), "launches": launches},
                 "gpu_launches": 2 * launches * args.steps, "clocks": clk}
+        line.update(extra)
     else:
         raise SystemExit(f"unknown workload {name!r}")
     print(json.dumps(line), flush=True)

@@ -12,6 +12,8 @@
  *   [PACK]  flashinfer.comm API reference, "Head-Chunk Layout and Transport
  *           Primitives", pack_ulysses_qkv_head_chunk.
  *   [MERGE] same section, merge_ulysses_output_head_chunk.
+ *   [XCHG]  flashinfer.comm API reference, UlyssesCommunicator.scatter_qkv_head_chunk,
+ *           gather_output_head_chunk and exchange_chunks.
  *   [PR5027] "allocation-stable, head-chunked Ulysses communication primitives"
  *           (flashinfer PR #5027), Description: uneven schedules, positive-stride
  *           non-contiguous views, storage-range alias checks, int32 limits.
@@ -262,6 +264,85 @@ qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor
 qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size,
                                               int local_heads, int head_offset, void* out,
                                               qnre_stream_t stream);
+
+/*
+ * ulysses_scatter_heads -- [ULY] scatter_heads for all P virtual ranks at once:
+ * [B, S_local, H, D] per rank -> [B, S_global, H_local, D] per rank, where rank r
+ * keeps heads [r*H_local, (r+1)*H_local) of the whole sequence:
+ *
+ *   out[r, b, r_s*S_local + s, hl, d] = x[r_s, b, s, r*H_local + hl, d]
+ *
+ *   x       device, contiguous [P, B, S_local, H, D] (rank r_s's shard first).
+ *   P       virtual ranks (>= 1), H % P == 0 (else QNRE_ERR_INVALID_ARG).  P == 1 copies.
+ *   dtype   qnre_dtype_t of x and out.
+ *   out     device, contiguous [P, B, P*S_local, H/P, D]; must not overlap x.
+ * P*B <= 65535.  B*S_local == 0 is an empty call.
+ */
+qnre_status_t ulysses_scatter_heads(const void* x, int P, int B, int S_local, int H, int D, int32_t dtype,
+                                    void* out, qnre_stream_t stream);
+
+/*
+ * ulysses_gather_heads -- [ULY] gather_heads for all P virtual ranks, the inverse
+ * of ulysses_scatter_heads:
+ *
+ *   out[r_s, b, s, r*H_local + hl, d] = y[r, b, r_s*S_local + s, hl, d]
+ *
+ *   y       device, contiguous [P, B, S_global, H_local, D]; S_global % P == 0.
+ *   out     device, contiguous [P, B, S_global/P, P*H_local, D]; must not overlap y.
+ */
+qnre_status_t ulysses_gather_heads(const void* y, int P, int B, int S_global, int H_local, int D, int32_t dtype,
+                                   void* out, qnre_stream_t stream);
+
+/*
+ * ulysses_pack_output_sequence_chunk -- the sequence split of one attention-output
+ * band that the output exchange sends ([XCHG] gather_output_head_chunk: the NCCL
+ * path packs the sequence split into staging; chunk r goes to rank r, which owns
+ * sequence rows [r*S_local, (r+1)*S_local)):
+ *
+ *   out[r, b, s, j, d] = x[b, r*S_local + s, j, d],   S_local = S_global / world_size
+ *
+ *   x           host pointer to a view [B, S_global, head_count, D], positive strides.
+ *   world_size  >= 1, divides S_global.
+ *   out         device, contiguous [world_size, B, S_local, head_count, D]; must not
+ *               overlap x.
+ */
+qnre_status_t ulysses_pack_output_sequence_chunk(const qnre_tensor4_t* x, int world_size, void* out,
+                                                 qnre_stream_t stream);
+
+/*
+ * ulysses_gather_output_head_chunk -- [XCHG] gather_output_head_chunk for all P
+ * virtual ranks at once: the sequence-split pack on every rank, the exchange and
+ * the merge into each rank's full output, as one copy.  Only the band is written:
+ *
+ *   out[r2, b, s, r*local_heads + head_offset + j, d] = x[r, b, r2*S_local + s, j, d]
+ *
+ *   x           device, contiguous [P, B, S_global, head_count, D]: rank r's attention
+ *               output band over the whole sequence.  S_global % P == 0.
+ *   local_heads, head_offset  0 <= head_offset, head_offset + head_count <= local_heads.
+ *   out         device, contiguous [P, B, S_global/P, P*local_heads, D]; other heads
+ *               keep their values; must not overlap x.
+ */
+qnre_status_t ulysses_gather_output_head_chunk(const void* x, int P, int B, int S_global, int head_count, int D,
+                                               int32_t dtype, int local_heads, int head_offset, void* out,
+                                               qnre_stream_t stream);
+
+/*
+ * ulysses_scatter_qkv_head_chunk -- [XCHG] scatter_qkv_head_chunk for all P virtual
+ * ranks at once: the head-chunk pack on every rank and the exchange of its
+ * destination slots, as one copy.  Rank r receives band
+ * [head_offset, head_offset + head_count) of its head slice for the whole sequence:
+ *
+ *   out[r, b, r_s*S_local + s, j, c*D + d] = X_c[r_s*B + b, s, r*H_local + head_offset + j, d]
+ *
+ *   q, k, v     host pointers to views [P*B, S_local, H, D] (rank r_s's batch rows
+ *               first), positive strides, equal shapes and dtype.
+ *   P           virtual ranks; P divides the first extent and H.
+ *   out         device, contiguous [P, B, P*S_local, head_count, 3*D]; must not overlap
+ *               q, k or v.
+ */
+qnre_status_t ulysses_scatter_qkv_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                                             const qnre_tensor4_t* v, int P, int head_offset, int head_count,
+                                             void* out, qnre_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

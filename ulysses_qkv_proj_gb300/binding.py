@@ -1,7 +1,10 @@
 """ctypes binding of libqnre (include/qnre.h).  Argument marshalling only.
 
-The names follow the C ABI: `qnre_forward`, `ulysses_pack_head_chunk`,
-`ulysses_merge_output_head_chunk`, plus the `Plan` wrapper around
+The names follow the C ABI: `qnre_forward`, `qnre_forward_noalloc`,
+`ulysses_pack_head_chunk`, `ulysses_merge_output_head_chunk`,
+`ulysses_scatter_heads`, `ulysses_gather_heads`,
+`ulysses_pack_output_sequence_chunk`, `ulysses_gather_output_head_chunk`,
+`ulysses_scatter_qkv_head_chunk`, plus the `Plan` wrapper around
 `qnre_plan_create` / `qnre_plan_destroy`.  Tensors are torch CUDA tensors;
 torch supplies device memory and the current stream, nothing else.  Every
 failure status raises `QnreError`; a missing library raises at first use.
@@ -73,6 +76,21 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ulysses_pack_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
     lib.ulysses_merge_output_head_chunk.restype = c_int
     lib.ulysses_merge_output_head_chunk.argtypes = [ctypes.POINTER(_Tensor4), c_int, c_int, c_int, c_vp, c_vp]
+    lib.qnre_forward_noalloc.restype = c_int
+    lib.qnre_forward_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_int, c_uint, c_int, c_int,
+                                         c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, ctypes.POINTER(_Out), c_vp, c_vp]
+    i32 = ctypes.c_int32
+    lib.ulysses_scatter_heads.restype = c_int
+    lib.ulysses_scatter_heads.argtypes = [c_vp, c_int, c_int, c_int, c_int, c_int, i32, c_vp, c_vp]
+    lib.ulysses_gather_heads.restype = c_int
+    lib.ulysses_gather_heads.argtypes = [c_vp, c_int, c_int, c_int, c_int, c_int, i32, c_vp, c_vp]
+    lib.ulysses_pack_output_sequence_chunk.restype = c_int
+    lib.ulysses_pack_output_sequence_chunk.argtypes = [ctypes.POINTER(_Tensor4), c_int, c_vp, c_vp]
+    lib.ulysses_gather_output_head_chunk.restype = c_int
+    lib.ulysses_gather_output_head_chunk.argtypes = [c_vp, c_int, c_int, c_int, c_int, c_int, i32, c_int, c_int,
+                                                     c_vp, c_vp]
+    lib.ulysses_scatter_qkv_head_chunk.restype = c_int
+    lib.ulysses_scatter_qkv_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
     _lib = lib
     return lib
 
@@ -189,6 +207,79 @@ def ulysses_merge_output_head_chunk(received, world_size: int, local_heads: int,
     _check(load_library().ulysses_merge_output_head_chunk(ctypes.byref(tr), world_size, local_heads,
                                                           head_offset, out.data_ptr(), _stream_ptr(stream)),
            "ulysses_merge_output_head_chunk")
+    return out
+
+
+def qnre_forward_noalloc(hidden: int, num_heads: int, P: int, x, w_qkv, q_norm_w, k_norm_w, cos_sin, positions,
+                         out: Dict[str, object], layout: str = "bshd", rope_style: str = "rotate_half",
+                         flags: int = 0, device_status=None, stream=None) -> None:
+    """qnre_forward without a plan: for callers that cannot allocate device memory when they
+    project.  device_status: optional int32 CUDA tensor of one element that receives the
+    call's QNRE_DEVICE_* bits."""
+    if x.dim() != 4 or x.shape[0] != P:
+        raise QnreError(1, "qnre_forward_noalloc: x must be [P, B, S_local, hidden]")
+    o = _Out(_ptr(out.get("q")), _ptr(out.get("k")), _ptr(out.get("v")), _ptr(out.get("fused")))
+    _check(load_library().qnre_forward_noalloc(hidden, num_heads, P, LAYOUTS.get(layout, -1),
+                                               ROPE_STYLES.get(rope_style, -1), flags, x.shape[1], x.shape[2],
+                                               x.data_ptr(), w_qkv.data_ptr(), q_norm_w.data_ptr(),
+                                               k_norm_w.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0],
+                                               _ptr(positions), ctypes.byref(o), _ptr(device_status),
+                                               _stream_ptr(stream)), "qnre_forward_noalloc")
+
+
+def _contig(t, where: str):
+    if not t.is_contiguous():
+        raise QnreError(1, f"{where}: tensor must be contiguous")
+    return t.data_ptr()
+
+
+def ulysses_scatter_heads(x, out, stream=None):
+    """x [P, B, S_local, H, D] -> out [P, B, P*S_local, H/P, D] (both contiguous)."""
+    P, B, S, H, D = x.shape
+    _check(load_library().ulysses_scatter_heads(_contig(x, "scatter_heads"), P, B, S, H, D, _dtype_code(x),
+                                                _contig(out, "scatter_heads"), _stream_ptr(stream)),
+           "ulysses_scatter_heads")
+    return out
+
+
+def ulysses_gather_heads(y, out, stream=None):
+    """y [P, B, S_global, H_local, D] -> out [P, B, S_global/P, P*H_local, D] (both contiguous)."""
+    P, B, S_g, H_l, D = y.shape
+    _check(load_library().ulysses_gather_heads(_contig(y, "gather_heads"), P, B, S_g, H_l, D, _dtype_code(y),
+                                               _contig(out, "gather_heads"), _stream_ptr(stream)),
+           "ulysses_gather_heads")
+    return out
+
+
+def ulysses_pack_output_sequence_chunk(x, world_size: int, out, stream=None):
+    """x view [B, S_global, head_count, D] -> out [world_size, B, S_global/world_size, head_count, D]."""
+    tx = _tensor4(x)
+    _check(load_library().ulysses_pack_output_sequence_chunk(ctypes.byref(tx), world_size,
+                                                             _contig(out, "pack_output_sequence_chunk"),
+                                                             _stream_ptr(stream)),
+           "ulysses_pack_output_sequence_chunk")
+    return out
+
+
+def ulysses_gather_output_head_chunk(x, local_heads: int, head_offset: int, out, stream=None):
+    """x [P, B, S_global, head_count, D] -> band head_offset of out [P, B, S_global/P, P*local_heads, D]."""
+    P, B, S_g, cnt, D = x.shape
+    _check(load_library().ulysses_gather_output_head_chunk(_contig(x, "gather_output_head_chunk"), P, B, S_g, cnt, D,
+                                                           _dtype_code(x), local_heads, head_offset,
+                                                           _contig(out, "gather_output_head_chunk"),
+                                                           _stream_ptr(stream)),
+           "ulysses_gather_output_head_chunk")
+    return out
+
+
+def ulysses_scatter_qkv_head_chunk(q, k, v, P: int, head_offset: int, head_count: int, out, stream=None):
+    """q/k/v views [P*B, S_local, H, D] -> out [P, B, P*S_local, head_count, 3*D] (contiguous)."""
+    tq, tk, tv = _tensor4(q), _tensor4(k), _tensor4(v)
+    _check(load_library().ulysses_scatter_qkv_head_chunk(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), P,
+                                                         head_offset, head_count,
+                                                         _contig(out, "scatter_qkv_head_chunk"),
+                                                         _stream_ptr(stream)),
+           "ulysses_scatter_qkv_head_chunk")
     return out
 
 

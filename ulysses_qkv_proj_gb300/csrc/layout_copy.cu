@@ -1,0 +1,140 @@
+// layout_copy.cu -- the head-row copy kernel behind the Ulysses layout entry
+// points ("Head-Chunk Layout and Transport Primitives" and "Ulysses
+// Context-Parallel All-to-All", flashinfer.comm API reference), for sm_103a.
+//
+// Every one of those transforms moves whole D-element head rows between two
+// layouts whose addresses are affine in (rank, head, batch, sequence), so one
+// kernel serves them all.  The grid is
+//   x: segment = (slot, component) head row,  y: runs of sequence rows,
+//   z: batch (split into two affine indices),
+// so blocks that run together cover every segment of the same rows and the
+// output is written as long contiguous runs.  Each thread copies 16-byte
+// vectors (when rows are 16-byte aligned with unit innermost stride) at a fixed
+// column of the segment while it walks the rows, so all index arithmetic is
+// hoisted out of the loop; four rows are in flight per thread.  Offsets are
+// 64-bit.
+#include "layout_copy.cuh"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace qnre {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+struct Args {
+  const char* src[3];
+  long long src_rank[3], src_head[3], src_z1[3], src_z0[3], src_s[3];
+  long long src_unit;
+  int src_head_offset;
+  char* dst;
+  long long dst_rank, dst_head, dst_comp, dst_z1, dst_z0, dst_s;
+  int dst_head_offset;
+  long long Z0, S;
+  int rows_per_block;
+  int head_count, comps, units;
+};
+
+template <typename U>
+__global__ void __launch_bounds__(kThreads) layout_copy_kernel(const Args a) {
+  const int seg = blockIdx.x;
+  const int c = seg % a.comps;
+  const int slot = seg / a.comps;
+  const int r = slot / a.head_count;
+  const int j = slot - r * a.head_count;
+  const long long z = blockIdx.z;
+  const long long z1 = z / a.Z0;
+  const long long z0 = z - z1 * a.Z0;
+  const long long s_begin = static_cast<long long>(blockIdx.y) * a.rows_per_block;
+  long long s_end = s_begin + a.rows_per_block;
+  if (s_end > a.S) s_end = a.S;
+
+  const char* src = a.src[c] + r * a.src_rank[c] + static_cast<long long>(a.src_head_offset + j) * a.src_head[c] +
+                    z1 * a.src_z1[c] + z0 * a.src_z0[c];
+  char* dst = a.dst + r * a.dst_rank + static_cast<long long>(a.dst_head_offset + j) * a.dst_head +
+              static_cast<long long>(c) * a.dst_comp + z1 * a.dst_z1 + z0 * a.dst_z0;
+  const long long ss = a.src_s[c];
+  const long long ds = a.dst_s;
+
+  if (a.units <= kThreads) {
+    const int rows_per_iter = kThreads / a.units;
+    const int lr = threadIdx.x / a.units;
+    const int u = threadIdx.x - lr * a.units;
+    if (lr >= rows_per_iter) return;
+    const char* sp = src + u * a.src_unit;
+    char* dp = dst + static_cast<long long>(u) * sizeof(U);
+    const long long step = rows_per_iter;
+    for (long long s = s_begin + lr; s < s_end; s += step * kUnroll) {
+      U v[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const long long sk = s + k * step;
+        if (sk < s_end) v[k] = *reinterpret_cast<const U*>(sp + sk * ss);
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const long long sk = s + k * step;
+        if (sk < s_end) *reinterpret_cast<U*>(dp + sk * ds) = v[k];
+      }
+    }
+  } else {
+    const long long n = (s_end - s_begin) * a.units;
+    for (long long e = threadIdx.x; e < n; e += kThreads) {
+      const long long s = s_begin + e / a.units;
+      const long long u = e % a.units;
+      *reinterpret_cast<U*>(dst + s * ds + u * static_cast<long long>(sizeof(U))) =
+          *reinterpret_cast<const U*>(src + s * ss + u * a.src_unit);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_layout_copy(const LayoutCopyPlan& p, cudaStream_t stream) {
+  if (p.S <= 0 || p.Z1 <= 0 || p.Z0 <= 0) return cudaSuccess;
+  Args a{};
+  for (int c = 0; c < 3; ++c) {
+    a.src[c] = static_cast<const char*>(p.src[c]);
+    a.src_rank[c] = p.src_rank[c];
+    a.src_head[c] = p.src_head[c];
+    a.src_z1[c] = p.src_z1[c];
+    a.src_z0[c] = p.src_z0[c];
+    a.src_s[c] = p.src_s[c];
+  }
+  a.src_unit = p.src_unit;
+  a.src_head_offset = p.src_head_offset;
+  a.dst = static_cast<char*>(p.dst);
+  a.dst_rank = p.dst_rank;
+  a.dst_head = p.dst_head;
+  a.dst_comp = p.dst_comp;
+  a.dst_z1 = p.dst_z1;
+  a.dst_z0 = p.dst_z0;
+  a.dst_s = p.dst_s;
+  a.dst_head_offset = p.dst_head_offset;
+  a.Z0 = p.Z0;
+  a.S = p.S;
+  a.head_count = p.head_count;
+  a.comps = p.comps;
+  a.units = p.units;
+
+  long long rows_per_block = 64;
+  while ((p.S + rows_per_block - 1) / rows_per_block > 65535) rows_per_block *= 2;
+  a.rows_per_block = static_cast<int>(rows_per_block);
+  const long long segments = static_cast<long long>(p.ranks) * p.head_count * p.comps;
+  const long long zs = p.Z1 * p.Z0;
+  if (segments > 0x7FFFFFFFll || zs > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>((p.S + rows_per_block - 1) / rows_per_block),
+                  static_cast<unsigned>(zs));
+  switch (p.unit_bytes) {
+    case 16: layout_copy_kernel<uint4><<<grid, kThreads, 0, stream>>>(a); break;
+    case 4: layout_copy_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(a); break;
+    case 2: layout_copy_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qnre

@@ -1,0 +1,37 @@
+// layout_copy.cuh -- launcher of the head-row copy kernel behind every Ulysses
+// layout entry point (head-chunk pack and merge, scatter/gather heads, the
+// output sequence-chunk pack and the composed head-chunk exchanges).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace qnre {
+
+// One launch copies head rows of `units` copy units each.  A "segment" is one
+// (slot, component) pair: slot = r*head_count + j names head j of rank r's
+// band, component c selects one of up to three sources (q | k | v).  Rows are
+// addressed by a sequence index s < S and a batch index z < Z1*Z0 split as
+// z = z1*Z0 + z0.  All strides are in bytes:
+//   src = src[c] + r*src_rank[c] + (src_head_offset + j)*src_head[c]
+//                + z1*src_z1[c] + z0*src_z0[c] + s*src_s[c] + u*src_unit
+//   dst = dst    + r*dst_rank    + (dst_head_offset + j)*dst_head + c*dst_comp
+//                + z1*dst_z1     + z0*dst_z0     + s*dst_s     + u*unit_bytes
+struct LayoutCopyPlan {
+  const void* src[3];
+  long long src_rank[3], src_head[3], src_z1[3], src_z0[3], src_s[3];
+  long long src_unit;
+  int src_head_offset;
+  void* dst;
+  long long dst_rank, dst_head, dst_comp, dst_z1, dst_z0, dst_s;
+  int dst_head_offset;
+  long long Z1, Z0, S;
+  int head_count;   // heads per band (j < head_count)
+  int ranks;        // r < ranks
+  int comps;        // 1 or 3
+  int units;        // copy units per head row
+  int unit_bytes;   // 16 (vector path), 4 or 2 (element path)
+};
+
+cudaError_t launch_layout_copy(const LayoutCopyPlan& plan, cudaStream_t stream);
+
+}  // namespace qnre

@@ -3,7 +3,7 @@
 // anything is enqueued, so a rejected call has no effect.
 #include "../../include/qnre.h"
 #include "fused_qkv.cuh"
-#include "head_chunk.cuh"
+#include "api_util.cuh"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -29,20 +29,14 @@ struct qnre_plan_s {
 
 namespace {
 
+using namespace qnre;
 using qnre::FusedArgs;
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-struct ByteRange {
-  uintptr_t lo, hi;  // [lo, hi)
-};
-
-bool overlaps(ByteRange a, ByteRange b) { return a.lo < b.hi && b.lo < a.hi; }
-
-ByteRange span(const void* p, uint64_t bytes) {
-  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-  return {lo, lo + static_cast<uintptr_t>(bytes)};
-}
+using api::aligned;
+using api::ByteRange;
+using api::from_cuda;
+using api::overlaps;
+using api::span;
 
 // ------------------------------------------------------------------ TMA maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -78,49 +72,6 @@ bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-int dtype_size(int32_t dt) {
-  switch (dt) {
-    case QNRE_DTYPE_BF16: return 2;
-    case QNRE_DTYPE_FP16: return 2;
-    case QNRE_DTYPE_FP32: return 4;
-    default: return 0;
-  }
-}
-
-// Checks common to every strided view; fills the byte span of its storage.
-qnre_status_t check_view(const qnre_tensor4_t* t, ByteRange* range) {
-  if (t == nullptr || t->data == nullptr) return QNRE_ERR_INVALID_ARG;
-  const int esz = dtype_size(t->dtype);
-  if (esz == 0) return QNRE_ERR_UNSUPPORTED;
-  // Batch and sequence extents may be 0 (an empty call); heads and head_dim may not.
-  bool empty = false;
-  uint64_t last = 0;
-  for (int i = 0; i < 4; ++i) {
-    if (t->shape[i] < (i < 2 ? 0 : 1) || t->stride[i] < 1) return QNRE_ERR_INVALID_ARG;
-    if (t->shape[i] > (int64_t{1} << 40) || t->stride[i] > (int64_t{1} << 40)) return QNRE_ERR_CAPACITY;
-    if (t->shape[i] == 0) {
-      empty = true;
-      continue;
-    }
-    last += static_cast<uint64_t>(t->shape[i] - 1) * static_cast<uint64_t>(t->stride[i]);
-    if (last > (uint64_t{1} << 56)) return QNRE_ERR_CAPACITY;
-  }
-  if (!aligned(t->data, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
-  *range = empty ? ByteRange{0, 0} : span(t->data, (last + 1) * static_cast<uint64_t>(esz));
-  return QNRE_OK;
-}
-
-bool rows_vectorisable(const qnre_tensor4_t* t, int esz) {
-  if (t->stride[3] != 1) return false;
-  if ((t->shape[3] * esz) % 16 != 0) return false;
-  if (!aligned(t->data, 16)) return false;
-  for (int i = 0; i < 3; ++i)
-    if ((t->stride[i] * esz) % 16 != 0) return false;
-  return true;
-}
-
-qnre_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QNRE_OK : QNRE_ERR_CUDA; }
 
 }  // namespace
 
@@ -302,137 +253,6 @@ qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, un
   if (clear && cudaMemset(plan->d_status, 0, sizeof(unsigned)) != cudaSuccess) return QNRE_ERR_CUDA;
   *bits = host;
   return host ? QNRE_ERR_DEVICE : QNRE_OK;
-}
-
-qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const qnre_tensor4_t* v,
-                                      int world_size, int head_offset, int head_count, void* out,
-                                      qnre_stream_t stream) {
-  const qnre_tensor4_t* X[3] = {q, k, v};
-  ByteRange in[3];
-  for (int c = 0; c < 3; ++c) {
-    const qnre_status_t st = check_view(X[c], &in[c]);
-    if (st != QNRE_OK) return st;
-  }
-  for (int c = 1; c < 3; ++c) {
-    if (X[c]->dtype != q->dtype) return QNRE_ERR_INVALID_ARG;
-    for (int i = 0; i < 4; ++i)
-      if (X[c]->shape[i] != q->shape[i]) return QNRE_ERR_INVALID_ARG;
-  }
-  if (out == nullptr) return QNRE_ERR_INVALID_ARG;
-  const int64_t B = q->shape[0], S = q->shape[1], H = q->shape[2], D = q->shape[3];
-  if (world_size < 1 || H % world_size != 0) return QNRE_ERR_INVALID_ARG;
-  const int64_t H_local = H / world_size;
-  if (head_offset < 0 || head_count < 1 || head_offset + static_cast<int64_t>(head_count) > H_local)
-    return QNRE_ERR_INVALID_ARG;
-  if (B > 65535) return QNRE_ERR_CAPACITY;
-  const int esz = dtype_size(q->dtype);
-  if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
-  const int64_t slots = static_cast<int64_t>(world_size) * head_count;
-  const uint64_t out_bytes = static_cast<uint64_t>(B) * S * slots * 3 * D * esz;
-  const ByteRange o = span(out, out_bytes);
-  for (int c = 0; c < 3; ++c)
-    if (overlaps(o, in[c])) return QNRE_ERR_ALIAS;
-
-  if (B == 0 || S == 0) return QNRE_OK;  // empty call
-  const bool vec = aligned(out, 16) && rows_vectorisable(q, esz) && rows_vectorisable(k, esz) &&
-                   rows_vectorisable(v, esz);
-  qnre::SegCopyPlan p{};
-  for (int c = 0; c < 3; ++c) {
-    p.src[c] = X[c]->data;
-    p.src_sb[c] = X[c]->stride[0] * esz;
-    p.src_ss[c] = X[c]->stride[1] * esz;
-    p.src_sh[c] = X[c]->stride[2] * esz;
-  }
-  p.unit_bytes = vec ? 16 : esz;
-  p.units = static_cast<int>(vec ? D * esz / 16 : D);
-  p.src_sd = vec ? 16 : q->stride[3] * esz;
-  // k and v must share q's innermost stride on the element path.
-  if (!vec && (k->stride[3] != q->stride[3] || v->stride[3] != q->stride[3])) {
-    // Fall back to one launch per component with its own stride.
-    for (int c = 0; c < 3; ++c) {
-      qnre::SegCopyPlan pc = p;
-      pc.src[0] = X[c]->data;
-      pc.src_sb[0] = p.src_sb[c];
-      pc.src_ss[0] = p.src_ss[c];
-      pc.src_sh[0] = p.src_sh[c];
-      pc.src_sd = X[c]->stride[3] * esz;
-      pc.dst = static_cast<char*>(out) + static_cast<int64_t>(c) * D * esz;
-      pc.dst_sb = S * slots * 3 * D * esz;
-      pc.dst_ss = slots * 3 * D * esz;
-      pc.B = B;
-      pc.S = S;
-      pc.comps = 1;
-      pc.segments = static_cast<int>(slots);
-      pc.head_count = head_count;
-      pc.src_heads_per_rank = static_cast<int>(H_local);
-      pc.src_head_offset = head_offset;
-      pc.dst_heads_per_rank = head_count;
-      pc.dst_head_offset = 0;
-      pc.dst_seg_bytes = 3 * D * esz;  // consecutive slots are 3*D elements apart
-      const cudaError_t e = qnre::launch_seg_copy(pc, reinterpret_cast<cudaStream_t>(stream));
-      if (e != cudaSuccess) return QNRE_ERR_CUDA;
-    }
-    return QNRE_OK;
-  }
-  p.dst = out;
-  p.dst_sb = S * slots * 3 * D * esz;
-  p.dst_ss = slots * 3 * D * esz;
-  p.B = B;
-  p.S = S;
-  p.comps = 3;
-  p.segments = static_cast<int>(slots * 3);
-  p.head_count = head_count;
-  p.src_heads_per_rank = static_cast<int>(H_local);
-  p.src_head_offset = head_offset;
-  p.dst_heads_per_rank = head_count;
-  p.dst_head_offset = 0;
-  p.dst_seg_bytes = D * esz;
-  return from_cuda(qnre::launch_seg_copy(p, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size, int local_heads,
-                                              int head_offset, void* out, qnre_stream_t stream) {
-  ByteRange in;
-  const qnre_status_t st = check_view(received, &in);
-  if (st != QNRE_OK) return st;
-  if (out == nullptr) return QNRE_ERR_INVALID_ARG;
-  const int64_t B = received->shape[0], S = received->shape[1], WC = received->shape[2], D = received->shape[3];
-  if (world_size < 1 || WC % world_size != 0) return QNRE_ERR_INVALID_ARG;
-  const int64_t head_count = WC / world_size;
-  if (local_heads < 1 || head_offset < 0 || head_offset + head_count > local_heads) return QNRE_ERR_INVALID_ARG;
-  if (B > 65535) return QNRE_ERR_CAPACITY;
-  const int esz = dtype_size(received->dtype);
-  if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
-  const int64_t out_heads = static_cast<int64_t>(world_size) * local_heads;
-  const ByteRange o = span(out, static_cast<uint64_t>(B) * S * out_heads * D * esz);
-  if (overlaps(o, in)) return QNRE_ERR_ALIAS;
-
-  if (B == 0 || S == 0) return QNRE_OK;  // empty call
-  const bool vec = aligned(out, 16) && rows_vectorisable(received, esz);
-  qnre::SegCopyPlan p{};
-  p.src[0] = p.src[1] = p.src[2] = received->data;
-  for (int c = 0; c < 3; ++c) {
-    p.src_sb[c] = received->stride[0] * esz;
-    p.src_ss[c] = received->stride[1] * esz;
-    p.src_sh[c] = received->stride[2] * esz;
-  }
-  p.unit_bytes = vec ? 16 : esz;
-  p.units = static_cast<int>(vec ? D * esz / 16 : D);
-  p.src_sd = vec ? 16 : received->stride[3] * esz;
-  p.dst = out;
-  p.dst_sb = S * out_heads * D * esz;
-  p.dst_ss = out_heads * D * esz;
-  p.B = B;
-  p.S = S;
-  p.comps = 1;
-  p.segments = static_cast<int>(WC);
-  p.head_count = static_cast<int>(head_count);
-  p.src_heads_per_rank = static_cast<int>(head_count);
-  p.src_head_offset = 0;
-  p.dst_heads_per_rank = local_heads;
-  p.dst_head_offset = head_offset;
-  p.dst_seg_bytes = D * esz;
-  return from_cuda(qnre::launch_seg_copy(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // --------------------------------------------------------------------------
