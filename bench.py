@@ -10,6 +10,9 @@ One step = one pass of the whole hot path over one batch of the workload
      [P*B, S_local, 3, 32, 128] projection buffer (all virtual ranks in one call);
   3. ulysses_merge_output_head_chunk of each packed band's q slice back into a
      [P*B, S_local, 32, 128] output (pack then merge reproduces q).
+Steps 2-3 do not depend on step 1, so they run on a second stream beside it
+(the memory-bound copies fill what the tensor-bound projection leaves idle);
+--no-overlap runs everything on one stream.
 The L2 (129 MB) is flushed with a 512 MB write between timed steps.
 
 value = tokens per second of the whole step (all ranks' tokens / step time).
@@ -183,21 +186,40 @@ def run_gpu(args):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(x_in, qkv_in, ev=None):
+    side = torch.cuda.Stream(device=dev)
+
+    primary = {"out": out, "packed": packed, "merged": merged}
+
+    def step(x_in, qkv_in, ev=None, bufs=None):
+        """ev = [start, fused done, pack done, merge done, step done] or None.
+
+        The fused op runs on the current stream; pack and merge (independent of it)
+        run on a second stream so they fill the SMs' spare issue slots and DRAM
+        bandwidth while the tensor cores work (--no-overlap serialises them)."""
+        bufs = bufs or primary
+        o_, p_, m_ = bufs["out"], bufs["packed"], bufs["merged"]
+        main = torch.cuda.current_stream()
+        start = ev[0] if ev else torch.cuda.Event()
+        start.record(main)
+        qb.qnre_forward(plan, x_in, w, qw, kw, cs, pos, o_, stream=main)
         if ev:
-            ev[0].record()
-        qb.qnre_forward(plan, x_in, w, qw, kw, cs, pos, out)
-        if ev:
-            ev[1].record()
+            ev[1].record(main)
+        tail = main if args.no_overlap else side
+        if tail is side:
+            side.wait_event(start)
         q, k, v = qkv_in[:, :, 0], qkv_in[:, :, 1], qkv_in[:, :, 2]
         for i, (off, cnt) in enumerate(SCHEDULE):
-            qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, packed[i])
+            qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, p_[i], stream=tail)
         if ev:
-            ev[2].record()
+            ev[2].record(tail)
         for i, (off, cnt) in enumerate(SCHEDULE):
-            qb.ulysses_merge_output_head_chunk(packed[i][..., :D], W, L, off, merged)
+            qb.ulysses_merge_output_head_chunk(p_[i][..., :D], W, L, off, m_, stream=tail)
         if ev:
-            ev[3].record()
+            ev[3].record(tail)
+        if tail is side:
+            main.wait_stream(side)
+        if ev:
+            ev[4].record(main)
 
     launches_per_step = 1 + 2 * len(SCHEDULE)
     for _ in range(args.warmup):
@@ -210,7 +232,7 @@ def run_gpu(args):
         raise RuntimeError("pack -> merge did not reproduce q")
 
     # ---- device-resident timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     if world > 1:
@@ -224,9 +246,9 @@ def run_gpu(args):
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     fused_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    pack_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pack_ms = [(e[1] if args.no_overlap else e[0]).elapsed_time(e[2]) for e in evs]
     merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     total_ms = sum(step_ms)
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -236,29 +258,53 @@ def run_gpu(args):
     tokens_per_step = wl.T
     value = tokens_per_step * world / (ms_per_step * 1e-3)
 
-    # ---- end to end: pinned host inputs in, results back to pinned host memory
-    out_host = {g: torch.empty_like(t, device="cpu").pin_memory() for g, t in out.items()}
-    merged_host = torch.empty_like(merged, device="cpu").pin_memory()
+    # ---- end to end: every step copies its inputs from pinned host memory and its
+    # results back.  Two buffer sets and separate copy streams let step i's
+    # device->host copy and step i+1's host->device copy overlap the compute.
+    sets = [primary, {"out": {g: torch.empty_like(t) for g, t in out.items()},
+                      "packed": [torch.empty_like(t) for t in packed], "merged": torch.empty_like(merged)}]
+    dev_in = [(torch.empty_like(x), torch.empty_like(qkv)) for _ in range(2)]
+    host_out = [({g: torch.empty_like(t, device="cpu").pin_memory() for g, t in out.items()},
+                 torch.empty_like(merged, device="cpu").pin_memory()) for _ in range(2)]
     h2d = x_host.numel() * 2 + qkv_host.numel() * 2
     d2h = sum(t.numel() * 2 for t in out.values()) + merged.numel() * 2
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    x_dev2 = torch.empty_like(x)
-    qkv_dev2 = torch.empty_like(qkv)
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n = args.steps
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_comp = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    main = torch.cuda.current_stream()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        e2e_ev[i][0].record()
-        x_dev2.copy_(x_host, non_blocking=True)
-        qkv_dev2.copy_(qkv_host, non_blocking=True)
-        step(x_dev2, qkv_dev2)
-        for g, t in out.items():
-            out_host[g].copy_(t, non_blocking=True)
-        merged_host.copy_(merged, non_blocking=True)
-        e2e_ev[i][1].record()
-        torch.cuda.synchronize()
-        flush.zero_()
+    e2e_start.record(main)
+    h2d_s.wait_event(e2e_start)
+    for i in range(n):
+        b = i % 2
+        xin, qin = dev_in[b]
+        if i >= 2:
+            h2d_s.wait_event(ev_comp[i - 2])   # step i-2 has finished reading this input set
+        with torch.cuda.stream(h2d_s):
+            xin.copy_(x_host, non_blocking=True)
+            qin.copy_(qkv_host, non_blocking=True)
+        ev_in[i].record(h2d_s)
+        main.wait_event(ev_in[i])
+        if i >= 2:
+            main.wait_event(ev_out[i - 2])     # this output set has been copied out
+        step(xin, qin, bufs=sets[b])
+        ev_comp[i].record(main)
+        d2h_s.wait_event(ev_comp[i])
+        ho, hm = host_out[b]
+        with torch.cuda.stream(d2h_s):
+            for g, t in sets[b]["out"].items():
+                ho[g].copy_(t, non_blocking=True)
+            hm.copy_(sets[b]["merged"], non_blocking=True)
+        ev_out[i].record(d2h_s)
+    main.wait_stream(d2h_s)
+    e2e_end.record(main)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    e2e_ms = e2e_start.elapsed_time(e2e_end) / n
+    if not torch.equal(host_out[(n - 1) % 2][1], qkv_host[:, :, 0]):
+        raise RuntimeError("end-to-end result differs")
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -290,6 +336,7 @@ def run_gpu(args):
                        "tokens_per_step": tokens_per_step, "P": wl.P, "B": wl.B, "S_local": wl.S,
                        "hidden": wl.hidden, "num_heads": wl.num_heads, "layout": wl.layout,
                        "schedule": [list(b) for b in SCHEDULE], "l2": "flushed (512 MB write) between steps",
+                       "streams": "one" if args.no_overlap else "fused on the main stream, pack/merge on a second",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": round(tflops / tc_peak, 4), "traffic": profiled_traffic(),
@@ -301,7 +348,9 @@ def run_gpu(args):
             "merge": {"ms": round(statistics.mean(merge_ms), 5), "bytes": merge_bytes, "GB/s": round(merge_gbs, 1),
                       "frac_hbm": round(merge_gbs / hbm_peak, 4), "launches": len(SCHEDULE)},
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "pipelined: step i's D2H and step i+1's H2D overlap compute; 268 MB of "
+                            "per-step copies exceed L2"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "wall_s_timed": round(t_wall, 4),
@@ -572,6 +621,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="run pack/merge after the fused op on one stream instead of beside it")
     ap.add_argument("--workload", default=None,
                     help="time one row alone on this workload instead of the headline step")
     args = ap.parse_args()
