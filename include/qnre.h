@@ -75,6 +75,8 @@ typedef enum { QNRE_DTYPE_BF16 = 0, QNRE_DTYPE_FP16 = 1, QNRE_DTYPE_FP32 = 2 } q
                                          were written as NaN and the table was not read */
 #define QNRE_DEVICE_WAIT_TIMEOUT 0x2u /* a pipeline wait inside the kernel ran past its time limit; the
                                          kernel stopped early and its outputs are incomplete */
+#define QNRE_DEVICE_READY_TIMEOUT 0x4u /* qnre_wait_ready gave up before every readiness word reached
+                                          its target */
 
 typedef struct qnre_plan_s* qnre_plan_t;
 
@@ -167,6 +169,43 @@ qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, 
                            const void* q_norm_w, const void* k_norm_w, const float* cos_sin,
                            int64_t n_pos, const int32_t* positions, const qnre_out_t* out,
                            qnre_stream_t stream);
+
+/*
+ * Readiness words ([FUSED], [MATH] "Description": the producer publishes
+ * per-chunk readiness words as it stores each destination's band, and a
+ * one-CTA wait kernel on a consumer stream acquires them).  Here one word per
+ * virtual rank counts the head rows stored into that rank's band.
+ *
+ * qnre_forward_publish -- qnre_forward that also publishes readiness.
+ *   ready   device, [P] uint32, 4-byte aligned, caller-owned; must not overlap any
+ *           input or output.  The call zeroes it in stream order, then the kernel
+ *           adds to ready[r] (release at GPU scope) each time an epilogue warp has
+ *           stored its rows of one head of rank r.  When the forward is complete,
+ *           every word equals qnre_ready_target(plan, B, S_local).
+ * Other arguments, checks and errors: as qnre_forward.
+ */
+qnre_status_t qnre_forward_publish(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+                                   const void* q_norm_w, const void* k_norm_w, const float* cos_sin,
+                                   int64_t n_pos, const int32_t* positions, const qnre_out_t* out,
+                                   unsigned* ready, qnre_stream_t stream);
+
+/* The value every readiness word reaches when a forward of (B, S_local) with this
+ * plan has stored all of that rank's band.  Host-only; no GPU work. */
+qnre_status_t qnre_ready_target(qnre_plan_t plan, int B, int S_local, unsigned* target);
+
+/*
+ * qnre_wait_ready -- enqueue on `stream` a one-CTA kernel that waits until every
+ * ready[r] (r < P) is >= target, with acquire loads, so work enqueued after it on
+ * `stream` sees the bands.  The wait is bounded: after timeout_ns (1 ns .. 10 s)
+ * it stops, raises QNRE_DEVICE_READY_TIMEOUT in the plan's status word and
+ * returns, leaving the context usable.
+ *   ready   device [P] uint32 written by qnre_forward_publish.
+ * A wait kernel that runs while its producer is still running (on another
+ * stream) depends on both being resident at once, which nothing guarantees on
+ * one GPU; order the wait after the producer unless the caller knows they fit.
+ */
+qnre_status_t qnre_wait_ready(qnre_plan_t plan, const unsigned* ready, unsigned target, uint64_t timeout_ns,
+                              qnre_stream_t stream);
 
 /* Read (and, if clear != 0, reset) the plan's device status bits
  * (QNRE_DEVICE_*).  Waits for `stream`, then copies 4 bytes to the host.

@@ -30,6 +30,7 @@ ROPE_STYLES = {"rotate_half": 0, "interleaved": 1}
 FLAG_EPILOGUE_OFF = 0x1
 DEVICE_BAD_POSITION = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
+DEVICE_READY_TIMEOUT = 0x4
 HEAD_DIM = 128
 
 
@@ -91,6 +92,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                                      c_vp, c_vp]
     lib.ulysses_scatter_qkv_head_chunk.restype = c_int
     lib.ulysses_scatter_qkv_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
+    lib.qnre_forward_publish.restype = c_int
+    lib.qnre_forward_publish.argtypes = [c_vp, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
+                                         ctypes.POINTER(_Out), c_vp, c_vp]
+    lib.qnre_ready_target.restype = c_int
+    lib.qnre_ready_target.argtypes = [c_vp, c_int, c_int, ctypes.POINTER(c_uint)]
+    lib.qnre_wait_ready.restype = c_int
+    lib.qnre_wait_ready.argtypes = [c_vp, c_vp, c_uint, ctypes.c_uint64, c_vp]
     _lib = lib
     return lib
 
@@ -208,6 +216,30 @@ def ulysses_merge_output_head_chunk(received, world_size: int, local_heads: int,
                                                           head_offset, out.data_ptr(), _stream_ptr(stream)),
            "ulysses_merge_output_head_chunk")
     return out
+
+
+def qnre_forward_publish(plan: Plan, x, w_qkv, q_norm_w, k_norm_w, cos_sin, positions, out: Dict[str, object],
+                         ready, stream=None) -> None:
+    """qnre_forward that also publishes per-destination readiness counts into ready (int32 CUDA [P])."""
+    if x.dim() != 4 or x.shape[0] != plan.P:
+        raise QnreError(1, "qnre_forward_publish: x must be [P, B, S_local, hidden]")
+    o = _Out(_ptr(out.get("q")), _ptr(out.get("k")), _ptr(out.get("v")), _ptr(out.get("fused")))
+    _check(load_library().qnre_forward_publish(plan.handle, x.shape[1], x.shape[2], x.data_ptr(), w_qkv.data_ptr(),
+                                               q_norm_w.data_ptr(), k_norm_w.data_ptr(), cos_sin.data_ptr(),
+                                               cos_sin.shape[0], _ptr(positions), ctypes.byref(o), ready.data_ptr(),
+                                               _stream_ptr(stream)), "qnre_forward_publish")
+
+
+def qnre_ready_target(plan: Plan, B: int, S_local: int) -> int:
+    t = ctypes.c_uint(0)
+    _check(load_library().qnre_ready_target(plan.handle, B, S_local, ctypes.byref(t)), "qnre_ready_target")
+    return t.value
+
+
+def qnre_wait_ready(plan: Plan, ready, target: int, timeout_ns: int, stream=None) -> None:
+    """Enqueue the bounded one-CTA wait for every ready[r] >= target; expiry sets DEVICE_READY_TIMEOUT."""
+    _check(load_library().qnre_wait_ready(plan.handle, ready.data_ptr(), target, timeout_ns, _stream_ptr(stream)),
+           "qnre_wait_ready")
 
 
 def qnre_forward_noalloc(hidden: int, num_heads: int, P: int, x, w_qkv, q_norm_w, k_norm_w, cos_sin, positions,

@@ -387,6 +387,12 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
           }
         }
       }
+      if (a.ready != nullptr) {
+        // This warp's 32 rows of the head are stored: publish them to rank r
+        // (release at GPU scope orders every lane's stores before the count).
+        __syncwarp();
+        if (lane == 0) ptx::red_add_release_gpu(a.ready + r, 1u);
+      }
     }
     if (bad_pos && valid) atomicOr(a.status, QNRE_DEVICE_BAD_POSITION);
 
@@ -511,6 +517,36 @@ cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fused_qkv_kernel, args);
+}
+
+}  // namespace qnre
+
+namespace qnre {
+namespace {
+
+// One CTA; thread r watches destination rank r's readiness count.  The wait is
+// bounded by the global timer, so a count that never arrives ends the kernel
+// with a status bit instead of a hang.
+__global__ void wait_ready_kernel(const unsigned* ready, int P, unsigned target, unsigned long long timeout_ns,
+                                  unsigned* status, unsigned timeout_bit) {
+  const int r = threadIdx.x;
+  if (r >= P) return;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (ptx::ld_acquire_gpu(ready + r) < target) {
+    if (ptx::global_timer_ns() - t0 > timeout_ns) {
+      atomicOr(status, timeout_bit);
+      return;
+    }
+    __nanosleep(256);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_ready(const unsigned* ready, int P, unsigned target, unsigned long long timeout_ns,
+                              unsigned* status, unsigned timeout_bit, cudaStream_t stream) {
+  wait_ready_kernel<<<1, ((P + 31) / 32) * 32, 0, stream>>>(ready, P, target, timeout_ns, status, timeout_bit);
+  return cudaGetLastError();
 }
 
 }  // namespace qnre

@@ -41,6 +41,7 @@ struct FusedArgs {
   uint16_t* out_v;
   uint16_t* out_fused;
   unsigned* status;
+  unsigned* ready;  // per destination rank, or null: per-warp head-row publication counts
   long long n_pos;
   int T, K, N, H, H_local, P, B, S;
   int layout;       // 0 bshd, 1 fused
@@ -51,6 +52,17 @@ struct FusedArgs {
 
 // Enqueue the fused kernel: `pairs` CTA pairs walk the tile list persistently.
 cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream);
+
+// Readiness count a complete forward publishes to each destination rank:
+// every epilogue warp of every pair tile adds 1 per head of that rank it stored.
+inline unsigned long long ready_target(long long num_m_tiles, int H_local) {
+  return static_cast<unsigned long long>(num_m_tiles) * 2 /*CTAs*/ * 4 /*epilogue warps*/ * 3 /*q,k,v*/ * H_local;
+}
+
+// Enqueue a one-CTA wait: thread r spins (with acquire loads) until ready[r] >=
+// target or `timeout_ns` passes; on expiry it ORs `timeout_bit` into *status.
+cudaError_t launch_wait_ready(const unsigned* ready, int P, unsigned target, unsigned long long timeout_ns,
+                              unsigned* status, unsigned timeout_bit, cudaStream_t stream);
 
 // One-time per-device kernel setup (shared-memory opt-in); returns in
 // *max_pairs how many CTA pairs of this kernel fit on the current device at once.

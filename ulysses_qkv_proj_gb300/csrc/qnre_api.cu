@@ -149,9 +149,15 @@ qnre_status_t qnre_plan_destroy(qnre_plan_t plan) {
   return from_cuda(e);
 }
 
-qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+}  // extern "C"
+
+namespace {
+
+// The fused forward; `ready` (device [P] words, or null) receives the
+// per-destination publication counts.
+qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
                            const void* q_norm_w, const void* k_norm_w, const float* cos_sin, int64_t n_pos,
-                           const int32_t* positions, const qnre_out_t* out, qnre_stream_t stream) {
+                           const int32_t* positions, const qnre_out_t* out, unsigned* ready, qnre_stream_t stream) {
   if (plan == nullptr || out == nullptr) return QNRE_ERR_INVALID_ARG;
   if (B < 0 || S_local < 0) return QNRE_ERR_INVALID_ARG;
   const int64_t tokens_per_rank = static_cast<int64_t>(B) * S_local;
@@ -196,6 +202,14 @@ qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, 
     for (int j = i + 1; j < n_out; ++j)
       if (overlaps(outs[i], outs[j])) return QNRE_ERR_ALIAS;
   }
+  if (ready != nullptr) {
+    if (!aligned(ready, 4)) return QNRE_ERR_ALIGNMENT;
+    const ByteRange rr = span(ready, static_cast<uint64_t>(P) * 4);
+    for (const ByteRange& r : in)
+      if (r.hi > r.lo && overlaps(rr, r)) return QNRE_ERR_ALIAS;
+    for (int i = 0; i < n_out; ++i)
+      if (overlaps(rr, outs[i])) return QNRE_ERR_ALIAS;
+  }
 
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return QNRE_ERR_CUDA;
@@ -215,6 +229,7 @@ qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.out_v = static_cast<uint16_t*>(bshd ? out->v : nullptr);
   a.out_fused = static_cast<uint16_t*>(bshd ? nullptr : out->fused);
   a.status = plan->d_status;
+  a.ready = ready;
   a.n_pos = n_pos;
   a.T = static_cast<int>(T);
   a.K = static_cast<int>(K);
@@ -240,7 +255,50 @@ qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(m_tiles, (48ll << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
   const int pairs = std::min(a.num_tiles, plan->max_pairs);
+  if (ready != nullptr &&
+      cudaMemsetAsync(ready, 0, static_cast<size_t>(P) * 4, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QNRE_ERR_CUDA;
   return from_cuda(qnre::launch_fused_qkv(a, pairs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+qnre_status_t qnre_forward(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+                           const void* q_norm_w, const void* k_norm_w, const float* cos_sin, int64_t n_pos,
+                           const int32_t* positions, const qnre_out_t* out, qnre_stream_t stream) {
+  return forward_impl(plan, B, S_local, x, w_qkv, q_norm_w, k_norm_w, cos_sin, n_pos, positions, out, nullptr,
+                      stream);
+}
+
+qnre_status_t qnre_forward_publish(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
+                                   const void* q_norm_w, const void* k_norm_w, const float* cos_sin, int64_t n_pos,
+                                   const int32_t* positions, const qnre_out_t* out, unsigned* ready,
+                                   qnre_stream_t stream) {
+  if (ready == nullptr) return QNRE_ERR_INVALID_ARG;
+  return forward_impl(plan, B, S_local, x, w_qkv, q_norm_w, k_norm_w, cos_sin, n_pos, positions, out, ready,
+                      stream);
+}
+
+qnre_status_t qnre_ready_target(qnre_plan_t plan, int B, int S_local, unsigned* target) {
+  if (plan == nullptr || target == nullptr || B < 0 || S_local < 0) return QNRE_ERR_INVALID_ARG;
+  const int64_t T = static_cast<int64_t>(B) * S_local * plan->P;
+  const int64_t m_tiles = (T + qnre::kPairM - 1) / qnre::kPairM;
+  const unsigned long long t = qnre::ready_target(m_tiles, plan->H_local);
+  if (t > 0xFFFFFFFFull) return QNRE_ERR_CAPACITY;
+  *target = static_cast<unsigned>(t);
+  return QNRE_OK;
+}
+
+qnre_status_t qnre_wait_ready(qnre_plan_t plan, const unsigned* ready, unsigned target, uint64_t timeout_ns,
+                              qnre_stream_t stream) {
+  if (plan == nullptr || ready == nullptr) return QNRE_ERR_INVALID_ARG;
+  if (!aligned(ready, 4)) return QNRE_ERR_ALIGNMENT;
+  if (plan->P > 1024) return QNRE_ERR_CAPACITY;
+  if (timeout_ns == 0 || timeout_ns > 10ull * 1000ull * 1000ull * 1000ull) return QNRE_ERR_INVALID_ARG;
+  return from_cuda(qnre::launch_wait_ready(ready, plan->P, target, timeout_ns, plan->d_status,
+                                           QNRE_DEVICE_READY_TIMEOUT, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, unsigned* bits, int clear) {
