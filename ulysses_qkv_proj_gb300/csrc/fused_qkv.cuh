@@ -18,7 +18,10 @@ constexpr int kPairM = 2 * kBM;
 constexpr int kBN = 256;                      // columns per tile (two heads)
 constexpr int kBNHalf = kBN / 2;              // B columns held by each CTA
 constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
-constexpr int kStages = 6;
+#ifndef QNRE_FUSED_STAGES
+#define QNRE_FUSED_STAGES 6
+#endif
+constexpr int kStages = QNRE_FUSED_STAGES;  // 32 KiB per stage per CTA
 constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kABytes = kBM * kBK * 2;        // 16 KiB
 constexpr int kBBytes = kBNHalf * kBK * 2;    // 16 KiB

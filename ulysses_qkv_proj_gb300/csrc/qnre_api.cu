@@ -9,6 +9,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+
+#ifndef QNRE_RASTER_L2_MB
+#define QNRE_RASTER_L2_MB 48  // L2 share for the resident x panels of a row-tile group
+#endif
 #include <cstdint>
 #include <mutex>
 #include <new>
@@ -252,7 +256,8 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   // The group's x panels (256 rows x hidden each) stay resident in L2 while W
   // streams past; keep them to about 48 MB of the 129 MB L2.
   const int64_t panel_bytes = static_cast<int64_t>(qnre::kPairM) * K * 2;
-  a.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(m_tiles, (48ll << 20) / panel_bytes)));
+  a.group_m = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(m_tiles, (static_cast<int64_t>(QNRE_RASTER_L2_MB) << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
   const int pairs = std::min(a.num_tiles, plan->max_pairs);
   if (ready != nullptr &&
