@@ -40,6 +40,7 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPairM, kBN, /*b_mn_major=*/true);
+constexpr uint32_t kIdescHalf = ptx::idesc_bf16_f32(kPairM, kBNHalf, /*b_mn_major=*/true);
 constexpr uint64_t kDrainGraceNs = 50ull * 1000ull;  // in-flight TMA settles in microseconds
 
 struct SmemLayout {
@@ -93,6 +94,24 @@ __device__ __forceinline__ void tile_coords(int tile, const FusedArgs& a, int& m
   n_blk = within / gm;
 }
 
+// One work item: rows [m_blk*256, +256), columns [col0, col0 + width).
+struct Work {
+  int m_blk;
+  int col0;
+  int width;  // kBN or kBNHalf
+};
+
+__device__ __forceinline__ Work work_coords(int w, const FusedArgs& a) {
+  int m_blk, n_blk;
+  if (w < a.num_full) {
+    tile_coords(w, a, m_blk, n_blk);
+    return {m_blk, n_blk * kBN, kBN};
+  }
+  const int j = w - a.num_full;
+  tile_coords(a.num_full + (j >> 1), a, m_blk, n_blk);
+  return {m_blk, n_blk * kBN + (j & 1) * kBNHalf, kBNHalf};
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
@@ -133,11 +152,12 @@ __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile u
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   bool ok = true;
-  for (int tile = pair; ok && tile < a.num_tiles; tile += num_pairs) {
-    int m_blk, n_blk;
-    tile_coords(tile, a, m_blk, n_blk);
-    const int row0 = m_blk * kPairM + static_cast<int>(L.rank) * kBM;
-    const int col0 = n_blk * kBN + static_cast<int>(L.rank) * kBNHalf;
+  for (int w = pair; ok && w < a.num_work; w += num_pairs) {
+    const Work t = work_coords(w, a);
+    const int row0 = t.m_blk * kPairM + static_cast<int>(L.rank) * kBM;
+    const int bcols = t.width / 2;  // this CTA's share of the tile's columns
+    const int col0 = t.col0 + static_cast<int>(L.rank) * bcols;
+    const uint32_t tx = 2u * static_cast<uint32_t>(kABytes + bcols * kBK * 2);
     for (int kb = 0; kb < a.num_k_blocks; ++kb, ++g) {
       const uint32_t s = g % kStages;
       const uint32_t ph = (g / kStages) & 1u;
@@ -145,11 +165,10 @@ __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile u
         ok = false;
         break;
       }
-      if (L.rank == 0) ptx::mbar_arrive_expect_tx(L.full + 8 * s, 2 * kStageBytes);
+      if (L.rank == 0) ptx::mbar_arrive_expect_tx(L.full + 8 * s, tx);
       const uint32_t bar = full_leader + 8 * s;
       ptx::tma_load_2d_pair(L.a + s * kABytes, &a.tmap_x, bar, kb * kBK, row0, pol_x);
-#pragma unroll
-      for (int j = 0; j < kBNHalf / 64; ++j) {
+      for (int j = 0; j < bcols / 64; ++j) {
         ptx::tma_load_2d_pair(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, bar, col0 + j * 64, kb * kBK,
                               pol_w);
       }
@@ -183,9 +202,10 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
   bool ok = true;
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
-  for (int tile = pair; ok && tile < a.num_tiles; tile += num_pairs, ++it) {
+  for (int w = pair; ok && w < a.num_work; w += num_pairs, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
+    const uint32_t idesc = w < a.num_full ? kIdesc : kIdescHalf;
     if (!bounded_wait(L.tempty + 8 * acc, aph ^ 1u, L, abort_flag, a.status, true)) {
       ok = false;
       break;
@@ -210,7 +230,7 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
         // B: N-major, 64-column blocks of kBK rows x 128 B (LBO = 8 KiB apart),
         //    8-row k groups 1024 B apart; the k-th 16-row slice starts 2 KiB in.
         const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024);
-        ptx::umma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        ptx::umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
       }
       ptx::umma_commit_pair_multicast(L.empty + 8 * s, 0x3);  // frees the stage in both CTAs
     }
@@ -238,15 +258,14 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   uint32_t it = 0;
-  for (int tile = pair; tile < a.num_tiles; tile += num_pairs, ++it) {
+  for (int w = pair; w < a.num_work; w += num_pairs, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
     if (!bounded_wait(L.tfull + 8 * acc, aph, L, abort_flag, a.status, true)) break;
     ptx::tc_fence_after_sync();
 
-    int m_blk, n_blk;
-    tile_coords(tile, a, m_blk, n_blk);
-    const int t = m_blk * kPairM + static_cast<int>(L.rank) * kBM + row;
+    const Work tw = work_coords(w, a);
+    const int t = tw.m_blk * kPairM + static_cast<int>(L.rank) * kBM + row;
     const bool valid = t < a.T;
     const int s_loc = valid ? t % a.S : 0;
     const int tb = valid ? t / a.S : 0;
@@ -261,8 +280,8 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
     const long long dest_row = static_cast<long long>(r_s) * a.S + s_loc;  // global row in batch b
 
 #pragma unroll 1
-    for (int hh = 0; hh < kBN / 128; ++hh) {
-      const int ch = n_blk * (kBN / 128) + hh;  // head column index in [0, 3H)
+    for (int hh = 0; hh < tw.width / 128; ++hh) {
+      const int ch = tw.col0 / 128 + hh;  // head column index in [0, 3H)
       if (ch >= three_h) break;
       const int g = ch / a.H;
       const int h = ch - g * a.H;

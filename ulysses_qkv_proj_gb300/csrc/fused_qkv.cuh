@@ -51,10 +51,32 @@ struct FusedArgs {
   int rope_style;   // 0 rotate-half, 1 interleaved
   int epilogue_on;  // 0: bare projection
   int num_m_tiles, num_n_tiles, num_tiles, group_m, num_k_blocks;  // m tiles are 256 rows
+  // Work list: items [0, num_full) are whole 256x256 tiles in raster order; items
+  // [num_full, num_work) split the remaining tiles into 256x128 halves (one head
+  // each), so a short last round or a small problem spreads over more pairs.
+  int num_full, num_work;
 };
 
 // Enqueue the fused kernel: `pairs` CTA pairs walk the tile list persistently.
 cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream);
+
+// Split of num_tiles pair tiles over at most max_pairs pairs: how many stay
+// whole, and how many work items (whole + halves) that makes.
+inline void plan_work(int num_tiles, int max_pairs, int* num_full, int* num_work) {
+  if (2 * num_tiles <= max_pairs) {  // small problem: every tile in two halves
+    *num_full = 0;
+    *num_work = 2 * num_tiles;
+    return;
+  }
+  const int rem = num_tiles % max_pairs;
+  if (rem > 0 && 2 * rem <= max_pairs) {  // short last round: halve its tiles
+    *num_full = num_tiles - rem;
+    *num_work = *num_full + 2 * rem;
+    return;
+  }
+  *num_full = num_tiles;
+  *num_work = num_tiles;
+}
 
 // Readiness count a complete forward publishes to each destination rank:
 // every epilogue warp of every pair tile adds 1 per head of that rank it stored.

@@ -259,7 +259,8 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.group_m = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(m_tiles, (static_cast<int64_t>(QNRE_RASTER_L2_MB) << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
-  const int pairs = std::min(a.num_tiles, plan->max_pairs);
+  qnre::plan_work(a.num_tiles, plan->max_pairs, &a.num_full, &a.num_work);
+  const int pairs = std::min(a.num_work, plan->max_pairs);
   if (ready != nullptr &&
       cudaMemsetAsync(ready, 0, static_cast<size_t>(P) * 4, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return QNRE_ERR_CUDA;
