@@ -15,7 +15,7 @@
 //     a 256-token x 256-column tile (= 2 heads), tiles walked in a grouped
 //     raster so concurrent pairs share x and W panels in L2;
 //   * warp 0 of each CTA: one thread issues TMA loads of its 128 x-rows
-//     (K-major) and its 128 W-columns (N-major) into a 6-stage ring (128-byte
+//     (K-major) and its 128 W-columns (N-major) into a 5-stage ring (128-byte
 //     swizzle); both CTAs' loads complete on the leader CTA's stage barrier;
 //   * warp 1 of the leader: one thread issues tcgen05.mma.cta_group::2 (M=256,
 //     N=256, K=16, bf16 in, fp32 accumulate in each CTA's tensor memory),
@@ -23,9 +23,10 @@
 //     main loop of tile i+1; commits are multicast to both CTAs;
 //   * warps 2-5 of each CTA: epilogue; thread i owns TMEM lane i = token row i
 //     of that CTA's half, so a head's 128 values are thread-local: the RMS sum,
-//     the scale and both RoPE pairings need no cross-thread traffic; each
-//     thread writes its head row (256 contiguous bytes) straight to the band
-//     destination, then both CTAs release the accumulator on the leader.
+//     the scale and both RoPE pairings need no cross-thread traffic; the bf16
+//     rows go through a swizzled 8 KiB per-warp staging buffer so each store
+//     instruction writes two whole 256-byte head rows of the band destination;
+//     then both CTAs release the accumulator on the leader.
 //   * every mbarrier wait has a time limit; on expiry the kernel raises a
 //     status bit, tells the peer CTA to stop, drains its own in-flight copies
 //     and MMAs, frees its tensor memory and returns.
@@ -247,7 +248,7 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
 // Epilogue: TMEM -> registers -> norm / RoPE -> bf16 -> band destination.
 // --------------------------------------------------------------------------
 __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
-                             const float* norm_w, volatile uint32_t* abort_flag) {
+                             const float* norm_w, uint4* epi_stage, volatile uint32_t* abort_flag) {
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int sub = warp & 3;  // TMEM lane quarter this warp may access
@@ -255,6 +256,8 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   const int S_g = a.P * a.S;
   const int three_h = 3 * a.H;
   const uint32_t tempty_leader = ptx::mapa_shared(L.tempty, 0);
+  uint4* stage = epi_stage + (warp - 2) * (32 * 16);  // 32 rows x 256 B for this warp
+  uint4* stage_row = stage + lane * 16;
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   uint32_t it = 0;
@@ -388,24 +391,41 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
             hi[i] = __uint_as_float(0x7FC00000u);
           }
         }
-        if (valid) {
+        // Stage the bf16 row in this warp's buffer: row `lane`, 16-byte chunk
+        // c at chunk slot c ^ (lane & 15) so that neither these writes nor the
+        // row-wise reads below collide in the same banks.
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 u;
-            u.x = pack_bf16x2(lo[8 * j + 0], lo[8 * j + 1]);
-            u.y = pack_bf16x2(lo[8 * j + 2], lo[8 * j + 3]);
-            u.z = pack_bf16x2(lo[8 * j + 4], lo[8 * j + 5]);
-            u.w = pack_bf16x2(lo[8 * j + 6], lo[8 * j + 7]);
-            d4[c_lo / 8 + j] = u;
-            uint4 w;
-            w.x = pack_bf16x2(hi[8 * j + 0], hi[8 * j + 1]);
-            w.y = pack_bf16x2(hi[8 * j + 2], hi[8 * j + 3]);
-            w.z = pack_bf16x2(hi[8 * j + 4], hi[8 * j + 5]);
-            w.w = pack_bf16x2(hi[8 * j + 6], hi[8 * j + 7]);
-            d4[c_hi / 8 + j] = w;
-          }
+        for (int j = 0; j < 4; ++j) {
+          uint4 u;
+          u.x = pack_bf16x2(lo[8 * j + 0], lo[8 * j + 1]);
+          u.y = pack_bf16x2(lo[8 * j + 2], lo[8 * j + 3]);
+          u.z = pack_bf16x2(lo[8 * j + 4], lo[8 * j + 5]);
+          u.w = pack_bf16x2(lo[8 * j + 6], lo[8 * j + 7]);
+          stage_row[(c_lo / 8 + j) ^ (lane & 15)] = u;
+          uint4 w;
+          w.x = pack_bf16x2(hi[8 * j + 0], hi[8 * j + 1]);
+          w.y = pack_bf16x2(hi[8 * j + 2], hi[8 * j + 3]);
+          w.z = pack_bf16x2(hi[8 * j + 4], hi[8 * j + 5]);
+          w.w = pack_bf16x2(hi[8 * j + 6], hi[8 * j + 7]);
+          stage_row[(c_hi / 8 + j) ^ (lane & 15)] = w;
         }
       }
+      // Write the warp's 32 head rows back two rows per instruction: lanes
+      // 0-15 cover row 2i and lanes 16-31 row 2i+1, 256 contiguous bytes each.
+      __syncwarp();
+      {
+        const int half = lane >> 4;
+        const int chunk = lane & 15;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int src_row = 2 * i + half;
+          uint4* rd = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<long long>(d4), src_row));
+          const int rv = __shfl_sync(0xffffffffu, valid ? 1 : 0, src_row);
+          const uint4 u = stage[src_row * 16 + (chunk ^ (src_row & 15))];
+          if (rv) rd[chunk] = u;
+        }
+      }
+      __syncwarp();
       if (a.ready != nullptr) {
         // This warp's 32 rows of the head are stored: publish them to rank r
         // (release at GPU scope orders every lane's stores before the count).
@@ -443,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   L.abort = ptx::smem_addr(tmem_holder + 1);
   L.rank = ptx::cluster_ctarank();
   float* norm_w = reinterpret_cast<float*>(bar_ptr + kBarBytes);
+  uint4* epi_stage = reinterpret_cast<uint4*>(bar_ptr + kBarBytes + 2 * 128 * 4);  // 16-byte aligned
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -484,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
     if (lane == 0 && L.rank == 0) run_mma(args, L, tmem_base, abort_flag);
     __syncwarp();
   } else {
-    run_epilogue(args, L, tmem_base, norm_w, abort_flag);
+    run_epilogue(args, L, tmem_base, norm_w, epi_stage, abort_flag);
   }
 
   ptx::tc_fence_before_sync();

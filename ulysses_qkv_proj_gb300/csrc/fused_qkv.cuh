@@ -19,7 +19,7 @@ constexpr int kBN = 256;                      // columns per tile (two heads)
 constexpr int kBNHalf = kBN / 2;              // B columns held by each CTA
 constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
 #ifndef QNRE_FUSED_STAGES
-#define QNRE_FUSED_STAGES 6
+#define QNRE_FUSED_STAGES 5
 #endif
 constexpr int kStages = QNRE_FUSED_STAGES;  // 32 KiB per stage per CTA
 constexpr int kThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -29,8 +29,10 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = kBN;                 // fp32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator
 constexpr int kBarBytes = 256;                // mbarriers + small words
+constexpr int kEpiStageBytes = 4 * 32 * 256;  // one 32-row x 256 B bf16 head tile per epilogue warp
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
-                           2 * 128 * 4 /*norm weights*/;
+                           2 * 128 * 4 /*norm weights*/ + kEpiStageBytes;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a limit");
 
 struct FusedArgs {
   CUtensorMap tmap_x;  // bf16 [T, K], box 64 x 128, 128-byte swizzle
