@@ -86,6 +86,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(x: float) -> float:
+    """Largest x over the process group (the slowest rank's time); x itself with one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
         int(os.environ.get("LOCAL_RANK", "0"))
@@ -249,11 +261,7 @@ def run_gpu(args):
     pack_ms = [(e[1] if args.no_overlap else e[0]).elapsed_time(e[2]) for e in evs]
     merge_ms = [e[2].elapsed_time(e[3]) for e in evs]
     step_ms = [e[0].elapsed_time(e[4]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms))
     ms_per_step = total_ms / args.steps
     tokens_per_step = wl.T
     value = tokens_per_step * world / (ms_per_step * 1e-3)
@@ -305,10 +313,7 @@ def run_gpu(args):
     e2e_ms = e2e_start.elapsed_time(e2e_end) / n
     if not torch.equal(host_out[(n - 1) % 2][1], qkv_host[:, :, 0]):
         raise RuntimeError("end-to-end result differs")
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms)
     e2e_value = tokens_per_step * world / (e2e_ms * 1e-3)
 
     # ---- rooflines
@@ -442,7 +447,7 @@ def run_reference(args):
     # size each step so that warm-up + timed steps take about 90 s of CPU time
     n_cal, dt_cal = cpu_sample_step(64)
     per_token = dt_cal / n_cal
-    budget = 90.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
     n = int(max(1, min(WORKLOAD.T, budget / per_token)))
     for _ in range(args.warmup):
         cpu_sample_step(n)
@@ -621,6 +626,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--ref-budget-s", type=float, default=90.0,
+                    help="CPU seconds the reference arm spreads over warm-up + timed steps")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run pack/merge after the fused op on one stream instead of beside it")
     ap.add_argument("--workload", default=None,
