@@ -12,3 +12,4 @@ the oracle itself (closed forms, invariants, brute force on tiny inputs and the
 hand-written fixtures under `tests/golden/`).  No function is "parity unpinned".
 """
 from .qnre_oracle import *  # noqa: F401,F403
+from .sage2_oracle import *  # noqa: F401,F403

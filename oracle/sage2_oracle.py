@@ -1,0 +1,171 @@
+"""Plain CPU oracle for the Sage2 low-precision QKV exchange (test infrastructure only).
+
+Source: flashinfer.comm API reference v0.7.4, "Prepared Low-Precision QKV
+Exchange" and UlyssesCommunicator.prepare_qkv / scatter_qkv, with the
+"Low-Precision Implementation Primitives" list: grouped INT8 Q/K and
+channel-scaled FP8 E4M3 V; FP32 statistics (a local K sum and V absolute
+maximum over the sequence, gathered across ranks); Q amax per global group of
+32 tokens, K amax of (K - global mean) per global group of 64 tokens; q, k INT8
+[B, S, H/P, D]; v FP8 E4M3 [B, D, H/P, S_pad]; Q/K scales FP32
+[B, H/P, width] with widths from the used sequence U; V scales FP32
+[B, H/P, D].
+
+Readings where the pages are silent (listed with reasons in the design notes):
+  * scale = amax / 127 (INT8) and amax / 448 (E4M3 maximum), FP32 division;
+    code = round-half-even(x / scale) (INT8 saturating to [-128, 127]; E4M3
+    nearest, ties to even, saturating at +-448); amax == 0 gives scale 0 and
+    code 0.
+  * K mean = (sum of K over the sequence) / U in FP32, the sum taken in a fixed
+    order: rows of a source rank in chunks of 256, each chunk summed row by row,
+    chunks in order, ranks in order.
+  * Rows at or beyond U get code 0 and take no part in any amax; S_pad = S
+    rounded up to a multiple of 64, padded with code 0.
+  * Group g of Q covers global rows [32 g, 32 g + 32); of K, [64 g, 64 g + 64).
+"""
+from __future__ import annotations
+
+from typing import Dict, List
+
+import numpy as np
+
+from .qnre_oracle import all_to_all, bf16_to_f64
+
+SUM_CHUNK = 256
+Q_GROUP = 32
+K_GROUP = 64
+V_PAD = 64
+INT8_DIV = np.float32(127.0)
+E4M3_MAX = np.float32(448.0)
+
+__all__ = ["e4m3_decode", "e4m3_encode", "int8_quantize", "sage2_k_sum", "sage2_scatter_qkv",
+           "SUM_CHUNK", "Q_GROUP", "K_GROUP", "V_PAD"]
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinity,
+# S.1111.111 is NaN, largest finite 448)
+# ---------------------------------------------------------------------------
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+_POS_CODES = np.arange(0x7F, dtype=np.uint8)          # 0x00 .. 0x7E: every finite non-negative value
+_POS_VALUES = e4m3_decode(_POS_CODES)
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 value (ties to the even code), saturating at +-448; NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    # brute force over the 127 finite magnitudes: the nearest, ties to the even mantissa
+    d = np.abs(a[..., None] - _POS_VALUES)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    even = (_POS_CODES & 1) == 0
+    pick = np.where(cand & even, 1, 0)
+    has_even = pick.any(axis=-1)
+    idx = np.where(has_even, np.argmax(pick, axis=-1), np.argmax(cand, axis=-1))
+    code = _POS_CODES[idx].astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code)  # the sign survives rounding to zero
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def int8_quantize(x: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """round-half-even(x / scale) in FP32, saturated to [-128, 127]; 0 where scale == 0."""
+    x = np.asarray(x, dtype=np.float32)
+    s = np.asarray(scale, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(np.float32(x) / s)
+    q = np.where(s == 0, 0, q)
+    return np.clip(q, -128, 127).astype(np.int8)
+
+
+# ---------------------------------------------------------------------------
+# Statistics
+# ---------------------------------------------------------------------------
+def sage2_k_sum(k_ranks: List[np.ndarray]) -> np.ndarray:
+    """FP32 sum of K over the global sequence, in the fixed order of the reading:
+    k_ranks[r] is rank r's [B, L, H, D]; returns [B, H, D] float32."""
+    total = None
+    for kr in k_ranks:
+        kf = bf16_to_f64(kr).astype(np.float32)
+        L = kf.shape[1]
+        rank_sum = np.zeros((kf.shape[0], kf.shape[2], kf.shape[3]), np.float32)
+        for c0 in range(0, L, SUM_CHUNK):
+            acc = np.zeros_like(rank_sum)
+            for s in range(c0, min(L, c0 + SUM_CHUNK)):
+                acc = (acc + kf[:, s]).astype(np.float32)
+            rank_sum = (rank_sum + acc).astype(np.float32)
+        total = rank_sum if total is None else (total + rank_sum).astype(np.float32)
+    return total
+
+
+def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ranks: List[np.ndarray],
+                      used_sequence: int) -> List[Dict[str, np.ndarray]]:
+    """Sage2 encoding after the head exchange, for every virtual rank.
+
+    q/k/v_ranks[r]: bf16 bits [B, L, H, D] of source rank r.  Returns, for each
+    destination rank r2 (heads [r2*H/P, (r2+1)*H/P)), a dict with
+    q, k: int8 [B, S, H/P, D]; v: E4M3 codes [B, D, H/P, S_pad];
+    q_scale [B, H/P, ceil(U/32)], k_scale [B, H/P, ceil(U/64)], v_scale [B, H/P, D] (float32).
+    """
+    P = len(q_ranks)
+    B, L, H, D = q_ranks[0].shape
+    if H % P:
+        raise ValueError("H must be divisible by P")
+    S = P * L
+    U = int(used_sequence)
+    if not 0 < U <= S:
+        raise ValueError("used_sequence must lie in (0, P*L]")
+    H_l = H // P
+    S_pad = -(-S // V_PAD) * V_PAD
+    wq, wk = -(-U // Q_GROUP), -(-U // K_GROUP)
+
+    # the exchange: rank r2 receives heads of its band for the whole sequence, in source-rank order
+    def exchange(xs):
+        sent = [[x[:, :, r2 * H_l:(r2 + 1) * H_l] for r2 in range(P)] for x in xs]
+        return [np.concatenate(rows, axis=1) for rows in all_to_all(sent)]   # [B, S, H_l, D] each
+
+    qg, kg, vg = exchange(q_ranks), exchange(k_ranks), exchange(v_ranks)
+    k_total = sage2_k_sum(k_ranks)                       # [B, H, D]
+    k_mean_all = (k_total / np.float32(U)).astype(np.float32)
+    out = []
+    live = np.arange(S) < U
+    for r2 in range(P):
+        qf = bf16_to_f64(qg[r2]).astype(np.float32)
+        kf = bf16_to_f64(kg[r2]).astype(np.float32)
+        vf = bf16_to_f64(vg[r2]).astype(np.float32)
+        k_mean = k_mean_all[:, r2 * H_l:(r2 + 1) * H_l]                     # [B, H_l, D]
+        ks = (kf - k_mean[:, None]).astype(np.float32)
+        q_scale = np.zeros((B, H_l, wq), np.float32)
+        k_scale = np.zeros((B, H_l, wk), np.float32)
+        q8 = np.zeros((B, S, H_l, D), np.int8)
+        k8 = np.zeros((B, S, H_l, D), np.int8)
+        for g in range(wq):
+            rows = slice(g * Q_GROUP, min(U, (g + 1) * Q_GROUP))
+            amax = np.abs(qf[:, rows]).max(axis=(1, 3))                       # [B, H_l]
+            sc = (amax / INT8_DIV).astype(np.float32)
+            q_scale[:, :, g] = sc
+            q8[:, rows] = int8_quantize(qf[:, rows], sc[:, None, :, None])
+        for g in range(wk):
+            rows = slice(g * K_GROUP, min(U, (g + 1) * K_GROUP))
+            amax = np.abs(ks[:, rows]).max(axis=(1, 3))
+            sc = (amax / INT8_DIV).astype(np.float32)
+            k_scale[:, :, g] = sc
+            k8[:, rows] = int8_quantize(ks[:, rows], sc[:, None, :, None])
+        vamax = np.where(live[None, :, None, None], np.abs(vf), 0).max(axis=1)   # [B, H_l, D]
+        v_scale = (vamax / E4M3_MAX).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            vq = np.where(v_scale[:, None] == 0, 0, vf / v_scale[:, None]).astype(np.float32)
+        v8 = np.where(live[None, :, None, None], e4m3_encode(vq), 0).astype(np.uint8)  # [B, S, H_l, D]
+        v_out = np.zeros((B, D, H_l, S_pad), np.uint8)
+        v_out[..., :S] = v8.transpose(0, 3, 2, 1)
+        out.append({"q": q8, "k": k8, "v": v_out, "q_scale": q_scale, "k_scale": k_scale, "v_scale": v_scale})
+    return out
