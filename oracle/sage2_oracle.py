@@ -37,7 +37,7 @@ V_PAD = 64
 INT8_DIV = np.float32(127.0)
 E4M3_MAX = np.float32(448.0)
 
-__all__ = ["e4m3_decode", "e4m3_encode", "int8_quantize", "sage2_k_sum", "sage2_scatter_qkv",
+__all__ = ["decode16", "e4m3_decode", "e4m3_encode", "int8_quantize", "sage2_k_sum", "sage2_scatter_qkv",
            "SUM_CHUNK", "Q_GROUP", "K_GROUP", "V_PAD"]
 
 
@@ -60,18 +60,17 @@ _POS_VALUES = e4m3_decode(_POS_CODES)
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
-    """Nearest E4M3 value (ties to the even code), saturating at +-448; NaN -> 0x7F."""
+    """Nearest E4M3 value (ties to the even code), saturating at +-448; NaN -> 0x7F.
+
+    The 127 finite magnitudes rise with their codes, so the nearest one is one of
+    the two neighbours found by a sorted search."""
     x = np.asarray(x, dtype=np.float64)
     a = np.minimum(np.abs(x), 448.0)
-    # brute force over the 127 finite magnitudes: the nearest, ties to the even mantissa
-    d = np.abs(a[..., None] - _POS_VALUES)
-    best = d.min(axis=-1, keepdims=True)
-    cand = d == best
-    even = (_POS_CODES & 1) == 0
-    pick = np.where(cand & even, 1, 0)
-    has_even = pick.any(axis=-1)
-    idx = np.where(has_even, np.argmax(pick, axis=-1), np.argmax(cand, axis=-1))
-    code = _POS_CODES[idx].astype(np.uint8)
+    i = np.clip(np.searchsorted(_POS_VALUES, a), 1, len(_POS_VALUES) - 1)
+    d_lo = a - _POS_VALUES[i - 1]
+    d_hi = _POS_VALUES[i] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((_POS_CODES[i] & 1) == 0))
+    code = _POS_CODES[np.where(take_hi, i, i - 1)].astype(np.uint8)
     code = np.where(np.signbit(x), code | 0x80, code)  # the sign survives rounding to zero
     code = np.where(np.isnan(x), 0x7F, code)
     return code.astype(np.uint8)
@@ -90,12 +89,21 @@ def int8_quantize(x: np.ndarray, scale: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Statistics
 # ---------------------------------------------------------------------------
-def sage2_k_sum(k_ranks: List[np.ndarray]) -> np.ndarray:
+def decode16(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    """bf16 or fp16 bit patterns (uint16) -> float32 (both convert exactly)."""
+    if dtype == "bf16":
+        return bf16_to_f64(bits).astype(np.float32)
+    if dtype == "fp16":
+        return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+    raise ValueError(f"unsupported input dtype {dtype!r}")
+
+
+def sage2_k_sum(k_ranks: List[np.ndarray], dtype: str = "bf16") -> np.ndarray:
     """FP32 sum of K over the global sequence, in the fixed order of the reading:
     k_ranks[r] is rank r's [B, L, H, D]; returns [B, H, D] float32."""
     total = None
     for kr in k_ranks:
-        kf = bf16_to_f64(kr).astype(np.float32)
+        kf = decode16(kr, dtype)
         L = kf.shape[1]
         rank_sum = np.zeros((kf.shape[0], kf.shape[2], kf.shape[3]), np.float32)
         for c0 in range(0, L, SUM_CHUNK):
@@ -108,10 +116,10 @@ def sage2_k_sum(k_ranks: List[np.ndarray]) -> np.ndarray:
 
 
 def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ranks: List[np.ndarray],
-                      used_sequence: int) -> List[Dict[str, np.ndarray]]:
+                      used_sequence: int, dtype: str = "bf16") -> List[Dict[str, np.ndarray]]:
     """Sage2 encoding after the head exchange, for every virtual rank.
 
-    q/k/v_ranks[r]: bf16 bits [B, L, H, D] of source rank r.  Returns, for each
+    q/k/v_ranks[r]: bf16 (or fp16) bits [B, L, H, D] of source rank r.  Returns, for each
     destination rank r2 (heads [r2*H/P, (r2+1)*H/P)), a dict with
     q, k: int8 [B, S, H/P, D]; v: E4M3 codes [B, D, H/P, S_pad];
     q_scale [B, H/P, ceil(U/32)], k_scale [B, H/P, ceil(U/64)], v_scale [B, H/P, D] (float32).
@@ -134,14 +142,14 @@ def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ra
         return [np.concatenate(rows, axis=1) for rows in all_to_all(sent)]   # [B, S, H_l, D] each
 
     qg, kg, vg = exchange(q_ranks), exchange(k_ranks), exchange(v_ranks)
-    k_total = sage2_k_sum(k_ranks)                       # [B, H, D]
+    k_total = sage2_k_sum(k_ranks, dtype)                # [B, H, D]
     k_mean_all = (k_total / np.float32(U)).astype(np.float32)
     out = []
     live = np.arange(S) < U
     for r2 in range(P):
-        qf = bf16_to_f64(qg[r2]).astype(np.float32)
-        kf = bf16_to_f64(kg[r2]).astype(np.float32)
-        vf = bf16_to_f64(vg[r2]).astype(np.float32)
+        qf = decode16(qg[r2], dtype)
+        kf = decode16(kg[r2], dtype)
+        vf = decode16(vg[r2], dtype)
         k_mean = k_mean_all[:, r2 * H_l:(r2 + 1) * H_l]                     # [B, H_l, D]
         ks = (kf - k_mean[:, None]).astype(np.float32)
         q_scale = np.zeros((B, H_l, wq), np.float32)

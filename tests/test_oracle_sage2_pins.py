@@ -42,6 +42,30 @@ def check_e4m3_rounding():
     assert enc(-1e-9) == 0x80                                           # sign kept when rounding to zero
 
 
+def _e4m3_brute_force(x):
+    """Nearest of all 127 finite magnitudes by exhaustive comparison (ties to the even code)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    mags = S2.e4m3_decode(np.arange(127, dtype=np.uint8))
+    out = []
+    for ai, xi in zip(a.ravel(), x.ravel()):
+        d = np.abs(ai - mags)
+        best = np.flatnonzero(d == d.min())
+        even = [c for c in best if c % 2 == 0]
+        c = even[0] if even else best[0]
+        out.append(c | (0x80 if np.signbit(xi) else 0))
+    return np.array(out, dtype=np.uint8).reshape(x.shape)
+
+
+def check_e4m3_matches_brute_force():
+    rng = np.random.default_rng(33)
+    mags = S2.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2                     # every tie point
+    x = np.concatenate([mids, -mids, rng.standard_normal(3000) * 50, rng.uniform(-500, 500, 1000),
+                        rng.standard_normal(500) * 0.01, [0.0, -0.0, 448.0, 1e9, -1e9]])
+    assert np.array_equal(S2.e4m3_encode(x), _e4m3_brute_force(x))
+
+
 def check_int8_quantize():
     q = S2.int8_quantize(np.array([2.5, 3.5, -2.5, -3.5, 0.49, 300.0, -300.0], np.float32), np.float32(1))
     assert q.tolist() == [2, 4, -2, -4, 0, 127, -128]
@@ -127,7 +151,13 @@ def check_sage2_smoothing_removes_channel_offset():
         assert not res[r]["k"].any() and not res[r]["k_scale"].any()
 
 
-CHECKS = [check_e4m3_rounding, check_int8_quantize, check_k_sum_exact_and_ordered,
+def check_decode16():
+    assert S2.decode16(np.array([0x3C00, 0xC000, 0x3555], np.uint16), "fp16").tolist() == [1.0, -2.0,
+                                                                                        np.float32(np.float16(1 / 3))]
+    assert S2.decode16(np.array([0x3F80], np.uint16), "bf16").tolist() == [1.0]
+
+
+CHECKS = [check_decode16, check_e4m3_rounding, check_e4m3_matches_brute_force, check_int8_quantize, check_k_sum_exact_and_ordered,
           check_sage2_structure_and_bounds, check_sage2_smoothing_removes_channel_offset]
 
 
@@ -153,13 +183,13 @@ def _mut_int8_floor(x, scale):
 def _mut_e4m3_ties_away(x):
     x = np.asarray(x, dtype=np.float64)
     a = np.minimum(np.abs(x), 448.0)
-    d = np.abs(a[..., None] - S2._POS_VALUES)
-    idx = np.argmax(np.where(d == d.min(axis=-1, keepdims=True), np.arange(127), -1), axis=-1)
-    code = S2._POS_CODES[idx].astype(np.uint8)
+    i = np.clip(np.searchsorted(S2._POS_VALUES, a), 1, 126)
+    take_hi = (S2._POS_VALUES[i] - a) <= (a - S2._POS_VALUES[i - 1])   # ties go up, not to even
+    code = S2._POS_CODES[np.where(take_hi, i, i - 1)].astype(np.uint8)
     return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
 
 
-def _mut_k_sum_no_chunks(k_ranks):
+def _mut_k_sum_no_chunks(k_ranks, dtype="bf16"):
     return np.stack([_f(k).astype(np.float32) for k in k_ranks]).sum(axis=(0, 2)).astype(np.float32) * np.float32(1.001)
 
 
