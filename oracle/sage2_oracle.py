@@ -11,10 +11,11 @@ maximum over the sequence, gathered across ranks); Q amax per global group of
 [B, H/P, D].
 
 Readings where the pages are silent (listed with reasons in the design notes):
-  * scale = amax / 127 (INT8) and amax / 448 (E4M3 maximum), FP32 division;
-    code = round-half-even(x / scale) (INT8 saturating to [-128, 127]; E4M3
-    nearest, ties to even, saturating at +-448); amax == 0 gives scale 0 and
-    code 0.
+  * stored scale = amax / 127 (INT8) or amax / 448 (E4M3 maximum), FP32
+    division; the codes use the reciprocal once per group or channel:
+    inv = 127 / amax (448 / amax), 0 when amax == 0, and code =
+    round-half-even(x * inv) in FP32 (INT8 saturating to [-128, 127]; E4M3
+    nearest, ties to even, saturating at +-448).
   * K mean = (sum of K over the sequence) / U in FP32, the sum taken in a fixed
     order: rows of a source rank in chunks of 256, each chunk summed row by row,
     chunks in order, ranks in order.
@@ -37,7 +38,8 @@ V_PAD = 64
 INT8_DIV = np.float32(127.0)
 E4M3_MAX = np.float32(448.0)
 
-__all__ = ["decode16", "e4m3_decode", "e4m3_encode", "int8_quantize", "sage2_k_sum", "sage2_scatter_qkv",
+__all__ = ["decode16", "e4m3_decode", "e4m3_encode", "int8_quantize", "reciprocal", "sage2_k_sum",
+           "sage2_scatter_qkv",
            "SUM_CHUNK", "Q_GROUP", "K_GROUP", "V_PAD"]
 
 
@@ -76,14 +78,20 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     return code.astype(np.uint8)
 
 
-def int8_quantize(x: np.ndarray, scale: np.ndarray) -> np.ndarray:
-    """round-half-even(x / scale) in FP32, saturated to [-128, 127]; 0 where scale == 0."""
+def int8_quantize(x: np.ndarray, inv_scale: np.ndarray) -> np.ndarray:
+    """round-half-even(x * inv_scale) in FP32, saturated to [-128, 127]."""
     x = np.asarray(x, dtype=np.float32)
-    s = np.asarray(scale, dtype=np.float32)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        q = np.rint(np.float32(x) / s)
-    q = np.where(s == 0, 0, q)
+    inv = np.asarray(inv_scale, dtype=np.float32)
+    q = np.rint((x * inv).astype(np.float32))
     return np.clip(q, -128, 127).astype(np.int8)
+
+
+def reciprocal(amax: np.ndarray, top: np.float32) -> np.ndarray:
+    """top / amax in FP32, 0 where amax == 0 (every code of that group or channel is 0)."""
+    a = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore"):
+        inv = (np.float32(top) / a).astype(np.float32)
+    return np.where(a > 0, inv, np.float32(0)).astype(np.float32)
 
 
 # ---------------------------------------------------------------------------
@@ -159,19 +167,16 @@ def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ra
         for g in range(wq):
             rows = slice(g * Q_GROUP, min(U, (g + 1) * Q_GROUP))
             amax = np.abs(qf[:, rows]).max(axis=(1, 3))                       # [B, H_l]
-            sc = (amax / INT8_DIV).astype(np.float32)
-            q_scale[:, :, g] = sc
-            q8[:, rows] = int8_quantize(qf[:, rows], sc[:, None, :, None])
+            q_scale[:, :, g] = (amax / INT8_DIV).astype(np.float32)
+            q8[:, rows] = int8_quantize(qf[:, rows], reciprocal(amax, INT8_DIV)[:, None, :, None])
         for g in range(wk):
             rows = slice(g * K_GROUP, min(U, (g + 1) * K_GROUP))
             amax = np.abs(ks[:, rows]).max(axis=(1, 3))
-            sc = (amax / INT8_DIV).astype(np.float32)
-            k_scale[:, :, g] = sc
-            k8[:, rows] = int8_quantize(ks[:, rows], sc[:, None, :, None])
+            k_scale[:, :, g] = (amax / INT8_DIV).astype(np.float32)
+            k8[:, rows] = int8_quantize(ks[:, rows], reciprocal(amax, INT8_DIV)[:, None, :, None])
         vamax = np.where(live[None, :, None, None], np.abs(vf), 0).max(axis=1)   # [B, H_l, D]
         v_scale = (vamax / E4M3_MAX).astype(np.float32)
-        with np.errstate(divide="ignore", invalid="ignore"):
-            vq = np.where(v_scale[:, None] == 0, 0, vf / v_scale[:, None]).astype(np.float32)
+        vq = (vf * reciprocal(vamax, E4M3_MAX)[:, None]).astype(np.float32)
         v8 = np.where(live[None, :, None, None], e4m3_encode(vq), 0).astype(np.uint8)  # [B, S, H_l, D]
         v_out = np.zeros((B, D, H_l, S_pad), np.uint8)
         v_out[..., :S] = v8.transpose(0, 3, 2, 1)
