@@ -590,7 +590,16 @@ def run_gpu_workload(args):
             g = nbytes / (ms * 1e-3) / 1e9
             return {"ms": round(ms, 5), "bytes": nbytes, "GB/s": round(g, 1), "frac_hbm": round(g / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), 4),
                     "launches": launches}
-        extra = {"scatter_heads": row(ms_sc, qbytes, 1), "gather_heads": row(ms_ga, qbytes, 1),
+        # Sage2 quantise-and-exchange of the same q/k/v (whole sequence used)
+        sage = qb.sage2_outputs(P, 1, S, wl.num_heads, D, P * S)
+        ms_sg, _ = timed(lambda: qb.ulysses_sage2_scatter_qkv(ranks[:, :, 0], ranks[:, :, 1], ranks[:, :, 2], P,
+                                                              P * S, sage))
+        n_el = 3 * P * S * wl.num_heads * D
+        extra_sage = row(ms_sg, n_el * 2 + n_el, 3)   # read bf16 q/k/v once, write 1-byte codes (scales < 0.1 %)
+        extra_sage["moved_bytes"] = n_el * 2 + n_el + (2 * n_el // 3) * 2   # + K and V read again by the statistics
+        extra_sage["note"] = "GB/s on algorithmic bytes; the statistics pass reads K and V a second time"
+        extra = {"sage2_scatter_qkv": extra_sage,
+                 "scatter_heads": row(ms_sc, qbytes, 1), "gather_heads": row(ms_ga, qbytes, 1),
                  "scatter_qkv_head_chunk": row(ms_sq, 3 * qbytes, len(wl.schedule)),
                  "gather_output_head_chunk": row(ms_go, qbytes, len(wl.schedule)),
                  "pack_output_sequence_chunk": row(ms_sp, qbytes // P, len(wl.schedule))}

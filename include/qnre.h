@@ -14,6 +14,9 @@
  *   [MERGE] same section, merge_ulysses_output_head_chunk.
  *   [XCHG]  flashinfer.comm API reference, UlyssesCommunicator.scatter_qkv_head_chunk,
  *           gather_output_head_chunk and exchange_chunks.
+ *   [LOWP]  flashinfer.comm API reference, "Prepared Low-Precision QKV Exchange"
+ *           (UlyssesCommunicator.prepare_qkv / scatter_qkv) and its
+ *           "Low-Precision Implementation Primitives" list.
  *   [PR5027] "allocation-stable, head-chunked Ulysses communication primitives"
  *           (flashinfer PR #5027), Description: uneven schedules, positive-stride
  *           non-contiguous views, storage-range alias checks, int32 limits.
@@ -382,6 +385,48 @@ qnre_status_t ulysses_gather_output_head_chunk(const void* x, int P, int B, int 
 qnre_status_t ulysses_scatter_qkv_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
                                              const qnre_tensor4_t* v, int P, int head_offset, int head_count,
                                              void* out, qnre_stream_t stream);
+
+/*
+ * Sage2 low-precision QKV exchange over P virtual ranks ([LOWP]): FP32
+ * statistics over the global sequence, INT8 Q per group of 32 tokens, INT8
+ * (K - global per-channel mean of K) per group of 64 tokens, FP8 E4M3 V with a
+ * per-channel scale, written into every destination rank's exchanged layout.
+ * Arithmetic (readings of the page): stored scale = amax / 127 (INT8) or
+ * amax / 448 (E4M3) in fp32; code = x * (127 / amax) (or x * (448 / amax))
+ * rounded to nearest even, saturated, the reciprocal taken once per group or
+ * channel and 0 when amax is 0; the K mean is sum / U, the sum taken in a fixed
+ * order (rows of a source rank in chunks of 256, chunks in order, ranks in
+ * order); rows at or beyond U are code 0 and take no part in any amax.
+ *
+ * ulysses_sage2_workspace_bytes -- bytes of scratch ulysses_sage2_scatter_qkv
+ * needs for (P, B, L, H, D); host-only, touches no device.
+ *
+ * ulysses_sage2_scatter_qkv --
+ *   q, k, v        host pointers to views [P*B, L, H, D] (rank r_s's batch rows first),
+ *                  bf16 or fp16, equal shapes; channel axis contiguous, every row and
+ *                  the base 16-byte aligned ([LOWP] scatter_qkv).  Rows at or beyond
+ *                  the used prefix must be zero (they enter the K sum).
+ *   P              virtual ranks, divides H and the first extent.  S = P*L.
+ *   used_sequence  U in (0, S].
+ *   q_out, k_out   device int8 [P, B, S, H/P, D], 16-byte aligned.
+ *   v_out          device E4M3 codes [P, B, D, H/P, S_pad], S_pad = S rounded up to 64,
+ *                  16-byte aligned; the padding is written as code 0.
+ *   q_scale        device fp32 [P, B, H/P, ceil(U/32)];  k_scale fp32 [P, B, H/P, ceil(U/64)];
+ *   v_scale        device fp32 [P, B, H/P, D].
+ *   workspace      device scratch of at least ulysses_sage2_workspace_bytes, 16-byte
+ *                  aligned, caller-owned; overwritten by the call.
+ * Every output element is written.  No output may overlap an input, another output
+ * or the workspace (QNRE_ERR_ALIAS).  D must be 64 or 128 (QNRE_ERR_UNSUPPORTED
+ * otherwise); S above 65535*64, P*B or H above 65535 give QNRE_ERR_CAPACITY.
+ * Three launches on `stream`; inputs must be finite.
+ */
+qnre_status_t ulysses_sage2_workspace_bytes(int P, int B, int L, int H, int D, uint64_t* bytes);
+
+qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                                        const qnre_tensor4_t* v, int P, int used_sequence, void* q_out,
+                                        void* k_out, void* v_out, float* q_scale, float* k_scale,
+                                        float* v_scale, void* workspace, uint64_t workspace_bytes,
+                                        qnre_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -166,3 +166,55 @@ def test_product_sources_do_not_reference_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_sage2_workspace_bytes(lib):
+    n = ctypes.c_uint64()
+    assert lib.ulysses_sage2_workspace_bytes(2, 1, 300, 4, 128, ctypes.byref(n)) == 0
+    chunks = 2   # 300 rows per rank in chunks of 256
+    assert n.value == (2 * 2 * chunks * 1 * 4 * 128 + 2 * 1 * 4 * 128) * 4
+    assert lib.ulysses_sage2_workspace_bytes(2, 1, 300, 4, 96, ctypes.byref(n)) == 2    # D not 64 / 128
+    assert lib.ulysses_sage2_workspace_bytes(3, 1, 300, 4, 128, ctypes.byref(n)) == 1   # H % P
+    assert lib.ulysses_sage2_workspace_bytes(2, 1, 0, 4, 128, ctypes.byref(n)) == 1
+    assert lib.ulysses_sage2_workspace_bytes(2, 1, 65535 * 32 + 1, 4, 128, ctypes.byref(n)) == 5
+    assert lib.ulysses_sage2_workspace_bytes(2, 1, 300, 4, 128, None) == 1
+
+
+def test_sage2_scatter_validation(lib):
+    """Every call here fails a host check, so nothing is launched (fake addresses)."""
+    P, B, L, H, D = 2, 1, 64, 4, 128
+    shp = [P * B, L, H, D]
+    st = _contig(shp)
+    n = P * B * L * H * D * 2
+    q, k, v = (_t4(BASE + i * n, shp, st) for i in range(3))
+    o = BASE + (1 << 30)
+    ws_n = ctypes.c_uint64()
+    assert lib.ulysses_sage2_workspace_bytes(P, B, L, H, D, ctypes.byref(ws_n)) == 0
+    mb = 1 << 20
+    outs = [o, o + 8 * mb, o + 16 * mb, o + 24 * mb, o + 25 * mb, o + 26 * mb, o + 27 * mb]
+
+    def call(q=q, k=k, v=v, P=P, U=P * L, outs=outs, ws=ws_n.value):
+        return lib.ulysses_sage2_scatter_qkv(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), P, U, *outs, ws,
+                                             None)
+    assert call(U=0) == 1
+    assert call(U=P * L + 1) == 1
+    assert call(P=3) == 1                                      # P does not divide the batch extent
+    assert call(ws=ws_n.value - 1) == 5                        # workspace too small
+    assert call(outs=outs[:6] + [None]) == 1
+    assert call(outs=[o + 8] + outs[1:]) == 3                  # q_out not 16-byte aligned
+    assert call(outs=outs[:2] + [o + 16 * mb + 4] + outs[3:]) == 3
+    assert call(outs=[BASE + 256] + outs[1:]) == 4             # q_out inside q
+    assert call(outs=outs[:1] + [o + 64] + outs[2:]) == 4      # k_out overlaps q_out
+    assert call(outs=outs[:6] + [o + 24 * mb]) == 4            # workspace overlaps q_scale
+    f32 = _t4(BASE, shp, st, dtype=2)
+    assert call(q=f32, k=f32, v=f32) == 2                      # fp32 inputs are not served
+    k16 = _t4(BASE + n, shp, st, dtype=1)
+    assert call(k=k16) == 1                                    # mixed dtypes
+    k96 = _t4(BASE + n, [P * B, L, H, 96], _contig([P * B, L, H, 96]))
+    assert call(k=k96) == 1                                    # shapes differ
+    q96 = _t4(BASE, [P * B, L, H, 96], _contig([P * B, L, H, 96]))
+    assert call(q=q96, k=q96, v=q96) == 2                      # D = 96
+    qs = _t4(BASE, shp, [st[0], st[1] + 4, st[2], 1])
+    assert call(q=qs) == 3                                     # row stride not a multiple of 16 bytes
+    qe = _t4(BASE, [P * B, 0, H, D], st)
+    assert call(q=qe, k=qe, v=qe) == 1                         # an empty sequence has no statistics

@@ -99,6 +99,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qnre_ready_target.argtypes = [c_vp, c_int, c_int, ctypes.POINTER(c_uint)]
     lib.qnre_wait_ready.restype = c_int
     lib.qnre_wait_ready.argtypes = [c_vp, c_vp, c_uint, ctypes.c_uint64, c_vp]
+    lib.ulysses_sage2_workspace_bytes.restype = c_int
+    lib.ulysses_sage2_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_uint64)]
+    lib.ulysses_sage2_scatter_qkv.restype = c_int
+    lib.ulysses_sage2_scatter_qkv.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int] + [c_vp] * 7 + \
+        [ctypes.c_uint64, c_vp]
     _lib = lib
     return lib
 
@@ -324,3 +329,41 @@ def alloc_outputs(plan: Plan, B: int, S_local: int, device="cuda") -> Dict[str, 
         return {g: torch.empty((plan.P, B, S_g, H_local, HEAD_DIM), dtype=torch.bfloat16, device=device)
                 for g in "qkv"}
     return {"fused": torch.empty((plan.P, B, S_g, H_local, 3 * HEAD_DIM), dtype=torch.bfloat16, device=device)}
+
+
+def ulysses_sage2_workspace_bytes(P: int, B: int, L: int, H: int, D: int) -> int:
+    """Scratch bytes ulysses_sage2_scatter_qkv needs for these sizes."""
+    n = ctypes.c_uint64()
+    _check(load_library().ulysses_sage2_workspace_bytes(P, B, L, H, D, ctypes.byref(n)),
+           "ulysses_sage2_workspace_bytes")
+    return n.value
+
+
+def sage2_outputs(P: int, B: int, L: int, H: int, D: int, used_sequence: int, device="cuda") -> Dict[str, object]:
+    """Output buffers (uninitialised) and the workspace for ulysses_sage2_scatter_qkv."""
+    import torch
+    S, H_l = P * L, H // P
+    S_pad = -(-S // 64) * 64
+    U = used_sequence
+    ws = ulysses_sage2_workspace_bytes(P, B, L, H, D)
+    return {"q": torch.empty((P, B, S, H_l, D), dtype=torch.int8, device=device),
+            "k": torch.empty((P, B, S, H_l, D), dtype=torch.int8, device=device),
+            "v": torch.empty((P, B, D, H_l, S_pad), dtype=torch.uint8, device=device),
+            "q_scale": torch.empty((P, B, H_l, -(-U // 32)), dtype=torch.float32, device=device),
+            "k_scale": torch.empty((P, B, H_l, -(-U // 64)), dtype=torch.float32, device=device),
+            "v_scale": torch.empty((P, B, H_l, D), dtype=torch.float32, device=device),
+            "workspace": torch.empty((ws,), dtype=torch.uint8, device=device)}
+
+
+def ulysses_sage2_scatter_qkv(q, k, v, P: int, used_sequence: int, out: Dict[str, object], stream=None):
+    """q/k/v views [P*B, L, H, D] (bf16 or fp16) -> the Sage2 codes and scales of every
+    destination rank in `out` (see sage2_outputs)."""
+    tq, tk, tv = _tensor4(q), _tensor4(k), _tensor4(v)
+    names = ("q", "k", "v", "q_scale", "k_scale", "v_scale")
+    ptrs = [_contig(out[n], "sage2_scatter_qkv") for n in names]
+    ws = out["workspace"]
+    _check(load_library().ulysses_sage2_scatter_qkv(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), P,
+                                                    used_sequence, *ptrs, _contig(ws, "sage2_scatter_qkv"),
+                                                    ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "ulysses_sage2_scatter_qkv")
+    return out

@@ -101,7 +101,7 @@ class HeadChunkWorkload:
         return self.num_heads // self.P
 
 
-# The five shapes. Names say what they are.
+# The shapes. Names say what they are.
 FUSED_WORKLOADS: Dict[str, FusedWorkload] = {
     "tiny_p2_s64_h4": FusedWorkload("tiny_p2_s64_h4", P=2, B=1, S=64, num_heads=4),
     "h4096_p4_s4096": FusedWorkload("h4096_p4_s4096", P=4, B=1, S=1024, num_heads=32),
@@ -113,6 +113,11 @@ FUSED_WORKLOADS: Dict[str, FusedWorkload] = {
 HEADCHUNK_WORKLOADS: Dict[str, HeadChunkWorkload] = {
     "headchunk_p2_s37760_h56": HeadChunkWorkload(
         "headchunk_p2_s37760_h56", P=2, B=1, S_global=37760, num_heads=56,
+        schedule=((0, 7), (7, 14), (21, 7))),
+    # the same heads over a 16k-token global sequence (q/k/v 0.7 GB): small enough
+    # for a per-kernel profile, still several times the L2
+    "headchunk_p2_s16384_h56": HeadChunkWorkload(
+        "headchunk_p2_s16384_h56", P=2, B=1, S_global=16384, num_heads=56,
         schedule=((0, 7), (7, 14), (21, 7))),
 }
 
