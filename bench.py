@@ -11,8 +11,11 @@ One step = one pass of the whole hot path over one batch of the workload
   3. ulysses_merge_output_head_chunk of each packed band's q slice back into a
      [P*B, S_local, 32, 128] output (pack then merge reproduces q).
 Steps 2-3 do not depend on step 1, so they run on a second stream beside it
-(the memory-bound copies fill what the tensor-bound projection leaves idle);
---no-overlap runs everything on one stream.
+(the memory-bound copies fill what the tensor-bound projection leaves idle).
+A copy CTA does not share an SM with a CTA of the persistent fused kernel, so
+the plan leaves --reserve-sms SMs (default 12) to the copies:
+qnre_plan_reserve_sms.  --no-overlap runs everything on one stream with every
+SM given to the fused kernel.
 The L2 (129 MB) is flushed with a 512 MB write between timed steps.
 
 value = tokens per second of the whole step (all ranks' tokens / step time).
@@ -186,6 +189,8 @@ def run_gpu(args):
     cs = torch.from_numpy(inp.cos_sin).to(dev)
     pos = torch.from_numpy(inp.positions).to(dev)
     plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
+    reserved = 0 if args.no_overlap else args.reserve_sms
+    plan.reserve_sms(reserved)
     out = qb.alloc_outputs(plan, wl.B, wl.S, dev)
 
     # head-chunk inputs: q/k/v views of a [P*B, S, 3, H, D] projection buffer
@@ -342,6 +347,7 @@ def run_gpu(args):
                        "hidden": wl.hidden, "num_heads": wl.num_heads, "layout": wl.layout,
                        "schedule": [list(b) for b in SCHEDULE], "l2": "flushed (512 MB write) between steps",
                        "streams": "one" if args.no_overlap else "fused on the main stream, pack/merge on a second",
+                       "reserved_sms": reserved,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": round(tflops / tc_peak, 4), "traffic": profiled_traffic(),
@@ -639,6 +645,8 @@ def main():
                     help="CPU seconds the reference arm spreads over warm-up + timed steps")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run pack/merge after the fused op on one stream instead of beside it")
+    ap.add_argument("--reserve-sms", type=int, default=12,
+                    help="SMs the fused kernel leaves to the concurrent pack/merge (overlapped step only)")
     ap.add_argument("--workload", default=None,
                     help="time one row alone on this workload instead of the headline step")
     args = ap.parse_args()

@@ -140,6 +140,19 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
 qnre_status_t qnre_plan_destroy(qnre_plan_t plan);
 
 /*
+ * qnre_plan_reserve_sms -- leave `sms` SMs (rounded up to whole CTA pairs) free
+ * of the fused kernel's persistent grid, for work the caller runs beside it on
+ * other streams (the pages' producers run "over every SM (no reserved SMs)"
+ * only on some architectures: [FUSED] Notes, per-architecture gates).  The
+ * fused kernel then runs on the remaining pairs; results are bit-identical for
+ * every setting (each tile's arithmetic does not depend on which pair runs it).
+ * 0 (the default) uses every SM.  Host-only; applies to later calls of this plan.
+ * Errors: QNRE_ERR_INVALID_ARG for a NULL plan, sms < 0, or a request that would
+ * leave no CTA pair.
+ */
+qnre_status_t qnre_plan_reserve_sms(qnre_plan_t plan, int sms);
+
+/*
  * qnre_forward -- the fused op on all P virtual ranks at once.  [FUSED], [MATH]:
  *   Y = x W (bf16 operands, fp32 accumulation) with W's columns grouped
  *   Q | K | V (column g*H*128 + h*128 + d);

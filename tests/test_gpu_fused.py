@@ -227,3 +227,31 @@ def test_full_size_sampled_values(name):
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_exact_placement(name):
     _exact_placement(WL.FUSED_WORKLOADS[name])
+
+
+def test_reserved_sms_give_identical_bits():
+    """qnre_plan_reserve_sms changes only how many CTA pairs run the tiles: the output
+    bits are the same for every setting, down to a single pair."""
+    wl = _wl("reserve", P=4, B=1, S=1024, H=32)          # 768 pair tiles: many rounds, a short last round
+    inp = WL.make_fused_inputs(wl)
+    d = _dev_inputs(inp)
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    results = []
+    for reserve in (0, 8, 16, 120, 0):                     # 120: 16 of the 76 pairs of a GB300 left
+        plan.reserve_sms(reserve)
+        out = qb.alloc_outputs(plan, wl.B, wl.S)
+        for t in out.values():
+            t.view(torch.int16).fill_(-1)
+        qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        results.append({g: to_host_bits(t) for g, t in out.items()})
+    for r in results[1:]:
+        for g in r:
+            assert np.array_equal(r[g], results[0][g]), g
+    for bad in (-1, sms, 2 * sms):
+        with pytest.raises(qb.QnreError) as e:
+            plan.reserve_sms(bad)
+        assert e.value.status == 1
+    _full_compare(wl, inp, {g: to_dev_bf16(b) for g, b in results[0].items()})

@@ -218,3 +218,7 @@ def test_sage2_scatter_validation(lib):
     assert call(q=qs) == 3                                     # row stride not a multiple of 16 bytes
     qe = _t4(BASE, [P * B, 0, H, D], st)
     assert call(q=qe, k=qe, v=qe) == 1                         # an empty sequence has no statistics
+
+
+def test_plan_reserve_sms_rejects_without_a_plan(lib):
+    assert lib.qnre_plan_reserve_sms(None, 8) == 1

@@ -68,6 +68,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qnre_plan_create.argtypes = [ctypes.POINTER(c_vp), c_int, c_int, c_int, c_int, c_int, c_i64, c_int, c_uint]
     lib.qnre_plan_destroy.restype = c_int
     lib.qnre_plan_destroy.argtypes = [c_vp]
+    lib.qnre_plan_reserve_sms.restype = c_int
+    lib.qnre_plan_reserve_sms.argtypes = [c_vp, c_int]
     lib.qnre_forward.restype = c_int
     lib.qnre_forward.argtypes = [c_vp, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
                                  ctypes.POINTER(_Out), c_vp]
@@ -181,6 +183,10 @@ class Plan:
                 load_library().qnre_plan_destroy(self._handle)
         except Exception:
             pass
+
+    def reserve_sms(self, sms: int) -> None:
+        """qnre_plan_reserve_sms: leave `sms` SMs free of the fused kernel (0 = use all)."""
+        _check(load_library().qnre_plan_reserve_sms(self._handle, sms), "qnre_plan_reserve_sms")
 
     def device_status(self, clear: bool = True, stream=None) -> int:
         bits = ctypes.c_uint(0)

@@ -27,7 +27,8 @@ struct qnre_plan_s {
   qnre_rope_t rope_style = QNRE_ROPE_ROTATE_HALF;
   unsigned flags = 0;
   int device = -1;
-  int max_pairs = 0;  // CTA pairs of the fused kernel resident at once
+  int max_pairs = 0;  // CTA pairs the fused kernel runs (all_pairs minus any reserved)
+  int all_pairs = 0;  // CTA pairs of the fused kernel that fit on the device at once
   unsigned* d_status = nullptr;
 };
 
@@ -141,7 +142,16 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
   p->flags = flags;
   p->device = dev;
   p->max_pairs = pairs;
+  p->all_pairs = pairs;
   *plan = p;
+  return QNRE_OK;
+}
+
+qnre_status_t qnre_plan_reserve_sms(qnre_plan_t plan, int sms) {
+  if (plan == nullptr || sms < 0) return QNRE_ERR_INVALID_ARG;
+  const int free_pairs = sms / 2 + sms % 2;  // SMs come free two at a time (one CTA pair)
+  if (free_pairs >= plan->all_pairs) return QNRE_ERR_INVALID_ARG;
+  plan->max_pairs = plan->all_pairs - free_pairs;
   return QNRE_OK;
 }
 
