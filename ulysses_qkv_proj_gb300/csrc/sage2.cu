@@ -7,8 +7,8 @@
 //
 // Three launches, each deterministic:
 //   1. stats_partial: one CTA per (16 or 32 heads, 256-row chunk of a source
-//      rank, batch); each thread owns 8 channels of one head (16-byte loads)
-//      and sums K / takes max|V| down them row by row;
+//      rank, batch); each thread owns 8 channels of one head (16-byte loads,
+//      eight rows in flight) and sums K / takes max|V| down them row by row;
 //   2. stats_final: one warp per (head, batch, 32 channels); thread d adds the chunk sums of
 //      each source rank in order, then the ranks in order -> K mean = sum / U,
 //      V scale = max / 448 and the V reciprocal 448 / max;
@@ -136,8 +136,11 @@ struct StatsArgs {
 // One CTA: one 256-row chunk of one source rank, 256 / (D / 8) heads.  Thread t
 // owns 8 channels (16 bytes) of one head and walks the chunk's rows in order,
 // so each column's sum is the same row-by-row fp32 sum the oracle takes.
+// kStatsRows rows of K and V are loaded before any is added (2 x 8 x 16 bytes
+// in flight per thread), enough to keep HBM busy even when the grid is small.
+constexpr int kStatsRows = 8;
 template <bool BF16>
-__global__ void __launch_bounds__(256) stats_partial_kernel(const StatsArgs a) {
+__global__ void __launch_bounds__(256, 2) stats_partial_kernel(const StatsArgs a) {
   const int tpr = a.D / 8;  // threads per head row
   const int h = blockIdx.x * (256 / tpr) + threadIdx.x / tpr;
   if (h >= a.H) return;
@@ -154,15 +157,15 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const StatsArgs a) {
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   uint4 vm = make_uint4(0, 0, 0, 0);
   int l = l0;
-  for (; l + 4 <= l1; l += 4) {
-    uint4 kw[4], vw[4];
+  for (; l + kStatsRows <= l1; l += kStatsRows) {
+    uint4 kw[kStatsRows], vw[kStatsRows];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kStatsRows; ++u) {
       kw[u] = *reinterpret_cast<const uint4*>(kp + static_cast<long long>(l + u) * a.k.ss);
       vw[u] = *reinterpret_cast<const uint4*>(vp + static_cast<long long>(l + u) * a.v.ss);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kStatsRows; ++u) {
       float f[8];
       unpack8<BF16>(kw[u], f);
 #pragma unroll
