@@ -523,6 +523,22 @@ def run_gpu_workload(args):
         ms, clk = timed(lambda: qb.qnre_forward(plan, x, w, qw, kw, cs, pos, out))
         if plan.device_status() != 0:
             raise RuntimeError("device status raised")
+        # readiness words: the publishing forward, then the bounded wait on a consumer
+        # stream ordered after it, joined back into the main stream
+        ready = torch.zeros((wl.P,), dtype=torch.int32, device=dev)
+        target = qb.qnre_ready_target(plan, wl.B, wl.S)
+        consumer = torch.cuda.Stream(device=dev)
+
+        def publish_and_wait():
+            main = torch.cuda.current_stream()
+            qb.qnre_forward_publish(plan, x, w, qw, kw, cs, pos, out, ready, stream=main)
+            consumer.wait_stream(main)
+            qb.qnre_wait_ready(plan, ready, target, 1_000_000_000, stream=consumer)
+            main.wait_stream(consumer)
+        ms_pub, _ = timed(lambda: qb.qnre_forward_publish(plan, x, w, qw, kw, cs, pos, out, ready))
+        ms_pw, _ = timed(publish_and_wait)
+        if plan.device_status() != 0 or ready.cpu().tolist() != [target] * wl.P:
+            raise RuntimeError("readiness words did not reach their target")
         tflops = wl.flops() / (ms * 1e-3) / 1e12
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         line = {"metric": "fused QKV+norm+RoPE+scatter tokens/s", "value": round(wl.T / (ms * 1e-3), 1),
@@ -532,6 +548,9 @@ def run_gpu_workload(args):
                            "l2": "flushed between launches"},
                 "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
                              "frac": round(tflops / peak, 4), "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                "readiness": {"forward_publish_ms": round(ms_pub, 5), "publish_and_wait_ms": round(ms_pw, 5),
+                              "publish_overhead_pct": round(100 * (ms_pub / ms - 1), 2),
+                              "note": "the wait kernel runs after the producer on a consumer stream"},
                 "gpu_launches": args.steps, "clocks": clk}
         plan.destroy()
     elif name in WL.HEADCHUNK_WORKLOADS:
