@@ -7,9 +7,13 @@ binding) never imports, calls or links anything here, and the two share no
 code: the only common module is the seeded input generator, which holds none
 of the method's arithmetic.
 
-Every function is pinned by `tests/test_oracle_pins.py` to facts fixed outside
-the oracle itself (closed forms, invariants, brute force on tiny inputs and the
-hand-written fixtures under `tests/golden/`).  No function is "parity unpinned".
+Every function is pinned by `tests/test_oracle_pins.py` and
+`tests/test_oracle_sage2_pins.py` to facts fixed outside the oracle itself
+(closed forms, invariants, brute force on tiny inputs and the hand-written
+fixtures under `tests/golden/`).  `pages_mode.py` is a diagnostic, not a parity
+reference: the pages' own fp32 test-reference form, pinned by
+`tests/test_oracle_pages_mode_pins.py` except for one step (the bf16 cast
+before the norm scale), which is "parity unpinned".
 """
 from .qnre_oracle import *  # noqa: F401,F403
 from .sage2_oracle import *  # noqa: F401,F403
