@@ -285,3 +285,32 @@ def test_meets_the_pages_own_bar(layout, rope):
         assert rest.mean() < 1e-4, f"{g}: {rest.sum()} elements beyond the pages' bar"
         closer = np.abs(got - exact[g]) < np.abs(r - exact[g])
         assert np.all(closer[rest]), f"{g}: beyond the bar where the reference form is the closer one"
+
+
+@pytest.mark.parametrize("P,H,S,B,layout,rope", [
+    (8, 24, 64, 1, "bshd", "interleaved"),    # hidden 3072 over 8 ranks: a band is 3 heads, pair tiles straddle bands
+    (2, 48, 96, 2, "fused", "rotate_half"),   # hidden 6144 over 2 ranks
+    (4, 64, 32, 1, "bshd", "rotate_half"),    # hidden 8192 over 4 ranks
+    (8, 32, 48, 1, "fused", "interleaved"),   # hidden 4096 over 8 ranks
+])
+def test_pages_grid_shapes_sampled(P, H, S, B, layout, rope):
+    """Shapes from the pages' measured grid (W in {2, 4, 8} x hidden in {3072, 4096,
+    6144, 8192}, head_dim 128) at short sequences: sampled tokens against the oracle,
+    every element written."""
+    wl = _wl("grid", P=P, B=B, S=S, H=H, layout=layout, rope=rope)
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    for t in out.values():
+        assert not bool(torch.isnan(t).any())
+    tok = sample_tokens(wl.T, wl.S, n=96)
+    x2 = inp.x.reshape(wl.T, wl.hidden)
+    O = oracle.project_norm_rope(x2[tok], inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin,
+                                 inp.positions.reshape(-1)[tok], wl.num_heads, wl.rope_style)
+    idx = torch.from_numpy(dest_index(tok, wl.P, wl.B, wl.S, wl.num_heads)).cuda()
+    for gi, g in enumerate("qkv"):
+        if wl.layout == "bshd":
+            got = out[g][idx[0], idx[1], idx[2], idx[3]]
+        else:
+            got = out["fused"][idx[0], idx[1], idx[2], idx[3]][..., gi * 128:(gi + 1) * 128]
+        assert_fused_close(to_host_f64(got), O[:, gi], what=f"grid P{P} H{H}/{g}")
