@@ -14,7 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
-from typing import Dict, List, Optional, Sequence
+from typing import Dict, List, Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqnre.so")
