@@ -13,7 +13,8 @@ One step = one pass of the whole hot path over one batch of the workload
 Steps 2-3 do not depend on step 1, so they run on a second stream beside it
 (the memory-bound copies fill what the tensor-bound projection leaves idle).
 A copy CTA does not share an SM with a CTA of the persistent fused kernel, so
-the plan leaves --reserve-sms SMs (default 12) to the copies:
+the plan leaves --reserve-sms SMs (default 4, one cluster of the fused kernel;
+with the 8 SMs its four-CTA clusters cannot use, the copies get 12) to them:
 qnre_plan_reserve_sms.  --no-overlap runs everything on one stream with every
 SM given to the fused kernel.
 The L2 (129 MB) is flushed with a 512 MB write between timed steps.
@@ -682,7 +683,7 @@ def main():
                     help="CPU seconds the reference arm spreads over warm-up + timed steps")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run pack/merge after the fused op on one stream instead of beside it")
-    ap.add_argument("--reserve-sms", type=int, default=12,
+    ap.add_argument("--reserve-sms", type=int, default=4,
                     help="SMs the fused kernel leaves to the concurrent pack/merge (overlapped step only)")
     ap.add_argument("--workload", default=None,
                     help="time one row alone on this workload instead of the headline step")

@@ -72,6 +72,16 @@ typedef enum { QNRE_DTYPE_BF16 = 0, QNRE_DTYPE_FP16 = 1, QNRE_DTYPE_FP32 = 2 } q
 #define QNRE_FLAG_EPILOGUE_OFF 0x1u /* store the bare projection for q, k and v (no norm, no RoPE).
                                        A diagnostic: with integer-coded inputs the result is exact,
                                        so band placement can be compared bit for bit. */
+#define QNRE_FLAG_W_MULTICAST 0x2u  /* always run the fused kernel in clusters of two CTA pairs
+                                       that take adjacent 256-row tiles of the same column tile
+                                       and share each W tile through one TMA multicast load.
+                                       Without this flag the plan still picks that form when it
+                                       fits and the row tiles pair up (an even count, or 16 or
+                                       more).  Results are bit-identical either way.
+                                       QNRE_ERR_UNSUPPORTED at plan creation if such clusters
+                                       cannot be resident. */
+#define QNRE_FLAG_ONE_PAIR 0x4u     /* always run the fused kernel one CTA pair per cluster (no
+                                       W multicast); not together with QNRE_FLAG_W_MULTICAST. */
 
 /* Device-side status bits (qnre_plan_device_status). */
 #define QNRE_DEVICE_BAD_POSITION 0x1u /* a token's position was outside [0, n_pos): its q and k rows
@@ -123,7 +133,8 @@ const char* qnre_status_string(qnre_status_t status);
  *   layout     QNRE_LAYOUT_BSHD or QNRE_LAYOUT_FUSED.
  *   max_tokens largest B*S_local per rank accepted by qnre_forward (>= 1).
  *   rope_style QNRE_ROPE_ROTATE_HALF or QNRE_ROPE_INTERLEAVED.
- *   flags      0 or QNRE_FLAG_EPILOGUE_OFF.
+ *   flags      0, or QNRE_FLAG_EPILOGUE_OFF and at most one of QNRE_FLAG_W_MULTICAST,
+ *              QNRE_FLAG_ONE_PAIR.
  *
  * Binds to the current CUDA device: queries it, sets the kernel's shared-memory
  * limit, and allocates the plan's 16-byte device status word (the only device

@@ -314,3 +314,34 @@ def test_pages_grid_shapes_sampled(P, H, S, B, layout, rope):
         else:
             got = out["fused"][idx[0], idx[1], idx[2], idx[3]][..., gi * 128:(gi + 1) * 128]
         assert_fused_close(to_host_f64(got), O[:, gi], what=f"grid P{P} H{H}/{g}")
+
+
+@pytest.mark.parametrize("S,B,H,P,layout,rope", [
+    (300, 1, 4, 2, "bshd", "rotate_half"),     # 600 tokens = 3 row tiles: the second pair of the last cluster idles
+    (200, 2, 8, 4, "fused", "interleaved"),    # 1600 tokens = 7 row tiles, 12 column tiles
+    (1024, 1, 32, 4, "bshd", "rotate_half"),   # the benchmarked shape: 16 row tiles, 48 column tiles
+])
+def test_w_multicast_bit_identical(S, B, H, P, layout, rope):
+    """Clusters of two CTA pairs sharing W through TMA multicast give the same bits as
+    one pair per cluster, and the same readiness counts (the 1600-token case ends
+    in a short round of half tiles)."""
+    wl = _wl("mcast", P=P, B=B, S=S, H=H, layout=layout, rope=rope)
+    inp = WL.make_fused_inputs(wl)
+    d = _dev_inputs(inp)
+    outs = []
+    for flags in (qb.FLAG_ONE_PAIR, qb.FLAG_W_MULTICAST):
+        plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style,
+                       flags=flags)
+        out = qb.alloc_outputs(plan, wl.B, wl.S)
+        for t in out.values():
+            t.view(torch.int16).fill_(-1)
+        ready = torch.zeros((wl.P,), dtype=torch.int32, device="cuda")
+        qb.qnre_forward_publish(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out, ready)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert ready.cpu().tolist() == [qb.qnre_ready_target(plan, wl.B, wl.S)] * wl.P
+        outs.append({g: to_host_bits(t) for g, t in out.items()})
+    for g in outs[0]:
+        assert np.array_equal(outs[1][g], outs[0][g]), g
+    if wl.T <= 1600:
+        _full_compare(wl, inp, {g: to_dev_bf16(b) for g, b in outs[1].items()})

@@ -53,6 +53,7 @@ def _plan_create(lib, hidden=512, heads=4, head_dim=128, P=2, layout=0, max_toke
     (dict(layout=7), 1),
     (dict(rope=5), 1),
     (dict(flags=0x80), 1),
+    (dict(flags=0x6), 1),               # W multicast and one pair per cluster together
     (dict(max_tokens=0), 1),
     (dict(max_tokens=1 << 31), 5),
 ])

@@ -28,6 +28,8 @@ STATUS_NAMES = {
 LAYOUTS = {"bshd": 0, "fused": 1}
 ROPE_STYLES = {"rotate_half": 0, "interleaved": 1}
 FLAG_EPILOGUE_OFF = 0x1
+FLAG_W_MULTICAST = 0x2
+FLAG_ONE_PAIR = 0x4
 DEVICE_BAD_POSITION = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 DEVICE_READY_TIMEOUT = 0x4

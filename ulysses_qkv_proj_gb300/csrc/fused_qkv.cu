@@ -53,12 +53,16 @@ struct SmemLayout {
   uint32_t tempty; // 2 mbarriers: epilogues of both CTAs -> MMA (leader)
   uint32_t drain;  // 1 mbarrier: MMA completion on abort (leader)
   uint32_t abort;  // abort word (shared address)
-  uint32_t rank;   // 0 = leader, 1 = peer
+  uint32_t rank;   // 0 = pair leader, 1 = peer
+  uint32_t crank;  // rank in the cluster (pair q = crank / 2)
+  uint32_t leader; // cluster rank of this CTA's pair leader
+  uint32_t ncta;   // CTAs in the cluster (2 or 4)
 };
 
 __device__ __forceinline__ void raise_abort(const SmemLayout& L, volatile uint32_t* abort_flag, unsigned* status) {
   *abort_flag = 1u;
-  ptx::st_shared_cluster_u32(ptx::mapa_shared(L.abort, L.rank ^ 1u), 1u);
+  for (uint32_t r = 0; r < L.ncta; ++r)
+    if (r != L.crank) ptx::st_shared_cluster_u32(ptx::mapa_shared(L.abort, r), 1u);
   atomicOr(status, QNRE_DEVICE_WAIT_TIMEOUT);
 }
 
@@ -85,11 +89,13 @@ __device__ __forceinline__ void grace_spin(uint64_t ns) {
   }
 }
 
-__device__ __forceinline__ void tile_coords(int tile, const FusedArgs& a, int& m_blk, int& n_blk) {
+// Raster position -> (row unit, column tile); a row unit is one 256-row tile,
+// or two adjacent ones when two pairs share a cluster.
+__device__ __forceinline__ void tile_coords(int tile, const FusedArgs& a, int num_m, int& m_blk, int& n_blk) {
   const int per_group = a.group_m * a.num_n_tiles;
   const int group = tile / per_group;
   const int first_m = group * a.group_m;
-  const int gm = min(a.group_m, a.num_m_tiles - first_m);
+  const int gm = min(a.group_m, num_m - first_m);
   const int within = tile - group * per_group;
   m_blk = first_m + within % gm;
   n_blk = within / gm;
@@ -102,14 +108,25 @@ struct Work {
   int width;  // kBN or kBNHalf
 };
 
-__device__ __forceinline__ Work work_coords(int w, const FusedArgs& a) {
+template <int kPC>
+__device__ __forceinline__ Work work_coords(int w, const FusedArgs& a, uint32_t pair_in_cluster) {
   int m_blk, n_blk;
+  if (kPC == 2) {  // work item = (row-tile pair, column tile); pair q takes row tile 2 * unit + q
+    const int q = static_cast<int>(pair_in_cluster);
+    if (w < a.num_full) {
+      tile_coords(w, a, a.num_mp_tiles, m_blk, n_blk);
+      return {2 * m_blk + q, n_blk * kBN, kBN};
+    }
+    const int j = w - a.num_full;
+    tile_coords(a.num_full + (j >> 1), a, a.num_mp_tiles, m_blk, n_blk);
+    return {2 * m_blk + q, n_blk * kBN + (j & 1) * kBNHalf, kBNHalf};
+  }
   if (w < a.num_full) {
-    tile_coords(w, a, m_blk, n_blk);
+    tile_coords(w, a, a.num_m_tiles, m_blk, n_blk);
     return {m_blk, n_blk * kBN, kBN};
   }
   const int j = w - a.num_full;
-  tile_coords(a.num_full + (j >> 1), a, m_blk, n_blk);
+  tile_coords(a.num_full + (j >> 1), a, a.num_m_tiles, m_blk, n_blk);
   return {m_blk, n_blk * kBN + (j & 1) * kBNHalf, kBNHalf};
 }
 
@@ -144,17 +161,19 @@ __device__ __forceinline__ void rotate(float& a, float& b, float c, float s) {
 // --------------------------------------------------------------------------
 // Producer (both CTAs): TMA loads of this CTA's x rows and W columns.
 // --------------------------------------------------------------------------
+template <int kPC>
 __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile uint32_t* abort_flag) {
   uint32_t g = 0;
   uint32_t used_mask = 0, parity_mask = 0;  // per stage: ever loaded / parity of its last load
   const uint64_t pol_x = ptx::l2_policy_evict_last();
   const uint64_t pol_w = ptx::l2_policy_evict_last();
-  const uint32_t full_leader = ptx::mapa_shared(L.full, 0);
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
+  const uint32_t full_leader = ptx::mapa_shared(L.full, L.leader);
+  const uint32_t q = L.crank >> 1;  // pair in the cluster
+  const int unit = blockIdx.x / (2 * kPC);
+  const int num_units = gridDim.x / (2 * kPC);
   bool ok = true;
-  for (int w = pair; ok && w < a.num_work; w += num_pairs) {
-    const Work t = work_coords(w, a);
+  for (int w = unit; ok && w < a.num_work; w += num_units) {
+    const Work t = work_coords<kPC>(w, a, q);
     const int row0 = t.m_blk * kPairM + static_cast<int>(L.rank) * kBM;
     const int bcols = t.width / 2;  // this CTA's share of the tile's columns
     const int col0 = t.col0 + static_cast<int>(L.rank) * bcols;
@@ -169,9 +188,19 @@ __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile u
       if (L.rank == 0) ptx::mbar_arrive_expect_tx(L.full + 8 * s, tx);
       const uint32_t bar = full_leader + 8 * s;
       ptx::tma_load_2d_pair(L.a + s * kABytes, &a.tmap_x, bar, kb * kBK, row0, pol_x);
-      for (int j = 0; j < bcols / 64; ++j) {
-        ptx::tma_load_2d_pair(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, bar, col0 + j * 64, kb * kBK,
-                              pol_w);
+      if (kPC == 2) {
+        // both pairs need this CTA's share of the W tile: pair q loads 64-column
+        // block q of it once, into this CTA and its counterpart in the other pair
+        // (a half tile has one block per CTA, loaded by pair 0)
+        const uint16_t mask = static_cast<uint16_t>((1u << L.rank) | (1u << (L.rank + 2)));
+        if (static_cast<int>(q) < bcols / 64)
+          ptx::tma_load_2d_pair_multicast(L.b + s * kBBytes + q * (64 * kBK * 2), &a.tmap_w, bar,
+                                          col0 + static_cast<int>(q) * 64, kb * kBK, mask, pol_w);
+      } else {
+        for (int j = 0; j < bcols / 64; ++j) {
+          ptx::tma_load_2d_pair(L.b + s * kBBytes + j * (64 * kBK * 2), &a.tmap_w, bar, col0 + j * 64, kb * kBK,
+                                pol_w);
+        }
       }
       used_mask |= 1u << s;
       parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
@@ -196,14 +225,19 @@ __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile u
 // MMA issuer (leader CTA only): tcgen05.mma over the stage ring into the TMEM
 // accumulators of both CTAs.
 // --------------------------------------------------------------------------
+template <int kPC>
 __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
                         volatile uint32_t* abort_flag) {
   uint32_t g = 0;
   uint32_t it = 0;
   bool ok = true;
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
-  for (int w = pair; ok && w < a.num_work; w += num_pairs, ++it) {
+  const int unit = blockIdx.x / (2 * kPC);
+  const int num_units = gridDim.x / (2 * kPC);
+  // a stage is free once every pair that reads it has consumed it: with two
+  // pairs the W blocks were multicast into all four CTAs
+  const uint16_t empty_mask = kPC == 2 ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * (L.crank >> 1)));
+  for (int w = unit; ok && w < a.num_work; w += num_units, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
     const uint32_t idesc = w < a.num_full ? kIdesc : kIdescHalf;
@@ -233,10 +267,10 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
         const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024);
         ptx::umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      ptx::umma_commit_pair_multicast(L.empty + 8 * s, 0x3);  // frees the stage in both CTAs
+      ptx::umma_commit_pair_multicast(L.empty + 8 * s, empty_mask);  // frees the stage
     }
     if (!ok) break;
-    ptx::umma_commit_pair_multicast(L.tfull + 8 * acc, 0x3);  // accumulators ready in both CTAs
+    ptx::umma_commit_pair_multicast(L.tfull + 8 * acc, pair_mask);  // accumulators ready in both CTAs
   }
   if (!ok) {
     ptx::umma_commit_pair(L.drain);
@@ -247,6 +281,7 @@ __device__ void run_mma(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_b
 // --------------------------------------------------------------------------
 // Epilogue: TMEM -> registers -> norm / RoPE -> bf16 -> band destination.
 // --------------------------------------------------------------------------
+template <int kPC>
 __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t tmem_base,
                              const float* norm_w, uint4* epi_stage, volatile uint32_t* abort_flag) {
   const int warp = threadIdx.x / 32;
@@ -255,19 +290,27 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   const int row = sub * 32 + lane;
   const int S_g = a.P * a.S;
   const int three_h = 3 * a.H;
-  const uint32_t tempty_leader = ptx::mapa_shared(L.tempty, 0);
+  const uint32_t tempty_leader = ptx::mapa_shared(L.tempty, L.leader);
   uint4* stage = epi_stage + (warp - 2) * (32 * 16);  // 32 rows x 256 B for this warp
   uint4* stage_row = stage + lane * 16;
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
+  const int unit = blockIdx.x / (2 * kPC);
+  const int num_units = gridDim.x / (2 * kPC);
   uint32_t it = 0;
-  for (int w = pair; w < a.num_work; w += num_pairs, ++it) {
+  for (int w = unit; w < a.num_work; w += num_units, ++it) {
     const uint32_t acc = it & 1u;
     const uint32_t aph = (it >> 1) & 1u;
     if (!bounded_wait(L.tfull + 8 * acc, aph, L, abort_flag, a.status, true)) break;
     ptx::tc_fence_after_sync();
 
-    const Work tw = work_coords(w, a);
+    const Work tw = work_coords<kPC>(w, a, L.crank >> 1);
+    if (kPC == 2 && tw.m_blk >= a.num_m_tiles) {
+      // the second pair's row tile past an odd tile count: its accumulator holds
+      // the product of zero rows; nothing is stored or published
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader + 8 * acc);
+      continue;
+    }
     const int t = tw.m_blk * kPairM + static_cast<int>(L.rank) * kBM + row;
     const bool valid = t < a.T;
     const int s_loc = valid ? t % a.S : 0;
@@ -442,6 +485,7 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   }
 }
 
+template <int kPC>
 __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_constant__ FusedArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -461,7 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kStages + 5));
   volatile uint32_t* abort_flag = tmem_holder + 1;
   L.abort = ptx::smem_addr(tmem_holder + 1);
-  L.rank = ptx::cluster_ctarank();
+  L.crank = ptx::cluster_ctarank();
+  L.rank = L.crank & 1u;
+  L.leader = L.crank & ~1u;
+  L.ncta = 2u * kPC;
   float* norm_w = reinterpret_cast<float*>(bar_ptr + kBarBytes);
   uint4* epi_stage = reinterpret_cast<uint4*>(bar_ptr + kBarBytes + 2 * 128 * 4);  // 16-byte aligned
 
@@ -473,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
     ptx::prefetch_tensormap(&args.tmap_w);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(L.full + 8 * s, 1);   // the leader's expect_tx arrival
-      ptx::mbar_init(L.empty + 8 * s, 1);  // one multicast commit
+      ptx::mbar_init(L.empty + 8 * s, kPC);  // one multicast commit from each pair that reads the stage
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(L.tfull + 8 * i, 1);   // one multicast commit
@@ -499,13 +546,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
-    if (lane == 0) run_producer(args, L, abort_flag);
+    if (lane == 0) run_producer<kPC>(args, L, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && L.rank == 0) run_mma(args, L, tmem_base, abort_flag);
+    if (lane == 0 && L.rank == 0) run_mma<kPC>(args, L, tmem_base, abort_flag);
     __syncwarp();
   } else {
-    run_epilogue(args, L, tmem_base, norm_w, epi_stage, abort_flag);
+    run_epilogue<kPC>(args, L, tmem_base, norm_w, epi_stage, abort_flag);
   }
 
   ptx::tc_fence_before_sync();
@@ -519,44 +566,60 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t prepare_fused_qkv_kernel(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fused_qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (sms / 2));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&clusters, fused_qkv_kernel, &cfg)) != cudaSuccess) return e;
-  if (clusters < 1) return cudaErrorInvalidConfiguration;
-  *max_pairs = clusters;
-  return cudaSuccess;
-}
+namespace {
 
-cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream) {
+template <int kPC>
+cudaLaunchConfig_t fused_config(int units, cudaLaunchAttribute* attr, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs);
+  cfg.gridDim = dim3(2 * kPC * units);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 2 * kPC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fused_qkv_kernel, args);
+  return cfg;
+}
+
+template <int kPC>
+cudaError_t max_clusters(int sms, int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(fused_qkv_kernel<kPC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = fused_config<kPC>(sms / (2 * kPC), attr, nullptr);
+  return cudaOccupancyMaxActiveClusters(clusters, fused_qkv_kernel<kPC>, &cfg);
+}
+
+}  // namespace
+
+cudaError_t prepare_fused_qkv_kernel(int* max_pairs, int* max_quads) {
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  int pairs = 0, quads = 0;
+  if ((e = max_clusters<1>(sms, &pairs)) != cudaSuccess) return e;
+  if (pairs < 1) return cudaErrorInvalidConfiguration;
+  if (max_clusters<2>(sms, &quads) != cudaSuccess) {
+    cudaGetLastError();  // four-CTA clusters unavailable: the one-pair kernel still serves
+    quads = 0;
+  }
+  *max_pairs = pairs;
+  *max_quads = quads;
+  return cudaSuccess;
+}
+
+cudaError_t launch_fused_qkv(const FusedArgs& args, int units, int pairs_per_cluster, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  if (pairs_per_cluster == 2) {
+    const cudaLaunchConfig_t cfg = fused_config<2>(units, attr, stream);
+    return cudaLaunchKernelEx(&cfg, fused_qkv_kernel<2>, args);
+  }
+  const cudaLaunchConfig_t cfg = fused_config<1>(units, attr, stream);
+  return cudaLaunchKernelEx(&cfg, fused_qkv_kernel<1>, args);
 }
 
 }  // namespace qnre

@@ -53,14 +53,18 @@ struct FusedArgs {
   int rope_style;   // 0 rotate-half, 1 interleaved
   int epilogue_on;  // 0: bare projection
   int num_m_tiles, num_n_tiles, num_tiles, group_m, num_k_blocks;  // m tiles are 256 rows
+  // Row units of the raster: num_m_tiles, or ceil(num_m_tiles / 2) when two
+  // pairs share a cluster and take adjacent row tiles of the same column tile.
+  int num_mp_tiles;
   // Work list: items [0, num_full) are whole 256x256 tiles in raster order; items
   // [num_full, num_work) split the remaining tiles into 256x128 halves (one head
   // each), so a short last round or a small problem spreads over more pairs.
   int num_full, num_work;
 };
 
-// Enqueue the fused kernel: `pairs` CTA pairs walk the tile list persistently.
-cudaError_t launch_fused_qkv(const FusedArgs& args, int pairs, cudaStream_t stream);
+// Enqueue the fused kernel: `units` clusters of `pairs_per_cluster` CTA pairs
+// (1, or 2 sharing W through TMA multicast) walk the work list persistently.
+cudaError_t launch_fused_qkv(const FusedArgs& args, int units, int pairs_per_cluster, cudaStream_t stream);
 
 // Split of num_tiles pair tiles over at most max_pairs pairs: how many stay
 // whole, and how many work items (whole + halves) that makes.
@@ -91,8 +95,9 @@ inline unsigned long long ready_target(long long num_m_tiles, int H_local) {
 cudaError_t launch_wait_ready(const unsigned* ready, int P, unsigned target, unsigned long long timeout_ns,
                               unsigned* status, unsigned timeout_bit, cudaStream_t stream);
 
-// One-time per-device kernel setup (shared-memory opt-in); returns in
-// *max_pairs how many CTA pairs of this kernel fit on the current device at once.
-cudaError_t prepare_fused_qkv_kernel(int* max_pairs);
+// One-time per-device kernel setup (shared-memory opt-in); returns how many
+// clusters of one CTA pair (*max_pairs) and of two pairs (*max_quads) fit on
+// the current device at once (*max_quads may be 0).
+cudaError_t prepare_fused_qkv_kernel(int* max_pairs, int* max_quads);
 
 }  // namespace qnre

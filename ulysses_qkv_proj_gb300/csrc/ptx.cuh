@@ -214,6 +214,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* 
       : "memory");
 }
 
+// The same load multicast to every CTA in `cta_mask` (same shared-memory offset
+// in each); each destination signals the mbarrier at `bar_cluster`'s offset in
+// the leader CTA of its own pair (cta_group::2).
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t smem_dst, const void* tmap,
+                                                           uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                           uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");

@@ -29,6 +29,8 @@ struct qnre_plan_s {
   int device = -1;
   int max_pairs = 0;  // CTA pairs the fused kernel runs (all_pairs minus any reserved)
   int all_pairs = 0;  // CTA pairs of the fused kernel that fit on the device at once
+  int max_quads = 0;  // the same for clusters of two pairs (QNRE_FLAG_W_MULTICAST)
+  int all_quads = 0;
   unsigned* d_status = nullptr;
 };
 
@@ -106,7 +108,8 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
   if (num_heads % P != 0) return QNRE_ERR_INVALID_ARG;
   if (layout != QNRE_LAYOUT_BSHD && layout != QNRE_LAYOUT_FUSED) return QNRE_ERR_INVALID_ARG;
   if (rope_style != QNRE_ROPE_ROTATE_HALF && rope_style != QNRE_ROPE_INTERLEAVED) return QNRE_ERR_INVALID_ARG;
-  if ((flags & ~QNRE_FLAG_EPILOGUE_OFF) != 0) return QNRE_ERR_INVALID_ARG;
+  if ((flags & ~(QNRE_FLAG_EPILOGUE_OFF | QNRE_FLAG_W_MULTICAST | QNRE_FLAG_ONE_PAIR)) != 0) return QNRE_ERR_INVALID_ARG;
+  if ((flags & QNRE_FLAG_W_MULTICAST) && (flags & QNRE_FLAG_ONE_PAIR)) return QNRE_ERR_INVALID_ARG;
   if (max_tokens < 1) return QNRE_ERR_INVALID_ARG;
   // The kernel's tile indices and TMA coordinates are 32-bit.
   if (max_tokens * static_cast<int64_t>(P) > (int64_t{1} << 31) - 256) return QNRE_ERR_CAPACITY;
@@ -118,7 +121,9 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return QNRE_ERR_CUDA;
   if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
-  if (qnre::prepare_fused_qkv_kernel(&pairs) != cudaSuccess) return QNRE_ERR_CUDA;
+  int quads = 0;
+  if (qnre::prepare_fused_qkv_kernel(&pairs, &quads) != cudaSuccess) return QNRE_ERR_CUDA;
+  if ((flags & QNRE_FLAG_W_MULTICAST) && quads < 1) return QNRE_ERR_UNSUPPORTED;
   if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
 
   qnre_plan_s* p = new (std::nothrow) qnre_plan_s();
@@ -143,6 +148,8 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
   p->device = dev;
   p->max_pairs = pairs;
   p->all_pairs = pairs;
+  p->max_quads = quads;
+  p->all_quads = quads;
   *plan = p;
   return QNRE_OK;
 }
@@ -152,6 +159,8 @@ qnre_status_t qnre_plan_reserve_sms(qnre_plan_t plan, int sms) {
   const int free_pairs = sms / 2 + sms % 2;  // SMs come free two at a time (one CTA pair)
   if (free_pairs >= plan->all_pairs) return QNRE_ERR_INVALID_ARG;
   plan->max_pairs = plan->all_pairs - free_pairs;
+  const int free_quads = sms / 4 + (sms % 4 != 0 ? 1 : 0);  // four SMs at a time with two pairs per cluster
+  plan->max_quads = plan->all_quads > free_quads ? plan->all_quads - free_quads : std::min(plan->all_quads, 1);
   return QNRE_OK;
 }
 
@@ -269,12 +278,29 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.group_m = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(m_tiles, (static_cast<int64_t>(QNRE_RASTER_L2_MB) << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
-  qnre::plan_work(a.num_tiles, plan->max_pairs, &a.num_full, &a.num_work);
-  const int pairs = std::min(a.num_work, plan->max_pairs);
+  // Clusters of two pairs sharing W through multicast: forced by the flag, else
+  // chosen when they fit and the row tiles pair up (an odd last row tile is
+  // paired with an empty one, so odd counts take it only when that waste is small).
+  const bool multicast =
+      !(plan->flags & QNRE_FLAG_ONE_PAIR) && plan->max_quads >= 1 &&
+      ((plan->flags & QNRE_FLAG_W_MULTICAST) || a.num_m_tiles % 2 == 0 || a.num_m_tiles >= 16);
+  int units = 0;
+  if (multicast) {
+    // work item = (pair of adjacent row tiles, column tile); a short last round
+    // is split into 256 x 128 halves like the one-pair kernel's
+    a.num_mp_tiles = (a.num_m_tiles + 1) / 2;
+    a.group_m = std::max(1, (a.group_m + 1) / 2);
+    qnre::plan_work(a.num_mp_tiles * a.num_n_tiles, plan->max_quads, &a.num_full, &a.num_work);
+    units = std::min(a.num_work, plan->max_quads);
+  } else {
+    a.num_mp_tiles = a.num_m_tiles;
+    qnre::plan_work(a.num_tiles, plan->max_pairs, &a.num_full, &a.num_work);
+    units = std::min(a.num_work, plan->max_pairs);
+  }
   if (ready != nullptr &&
       cudaMemsetAsync(ready, 0, static_cast<size_t>(P) * 4, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return QNRE_ERR_CUDA;
-  return from_cuda(qnre::launch_fused_qkv(a, pairs, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(qnre::launch_fused_qkv(a, units, multicast ? 2 : 1, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -365,12 +391,12 @@ qnre_status_t noalloc_setup(int dev, NoAllocDevice* out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   NoAllocDevice& st = g_noalloc_dev[dev];
   if (!st.ready) {
-    int major = 0, minor = 0, pairs = 0;
+    int major = 0, minor = 0, pairs = 0, quads = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return QNRE_ERR_CUDA;
     if (major != 10 || minor != 3) return QNRE_ERR_UNSUPPORTED;
-    if (qnre::prepare_fused_qkv_kernel(&pairs) != cudaSuccess) return QNRE_ERR_CUDA;
+    if (qnre::prepare_fused_qkv_kernel(&pairs, &quads) != cudaSuccess) return QNRE_ERR_CUDA;
     if (encode_tiled_fn() == nullptr) return QNRE_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return QNRE_ERR_CUDA;
