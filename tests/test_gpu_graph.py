@@ -16,7 +16,8 @@ from ulysses_qkv_proj_gb300 import binding as qb  # noqa: E402
 
 
 def test_forward_and_pack_merge_replay_with_fresh_inputs():
-    wl = WL.FusedWorkload("graph", P=2, B=2, S=160, num_heads=4, layout="fused", rope_style="interleaved")
+    # 1024 tokens = 4 row tiles: the plan takes clusters of two pairs sharing W (multicast)
+    wl = WL.FusedWorkload("graph", P=2, B=2, S=256, num_heads=4, layout="fused", rope_style="interleaved")
     plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, rope_style=wl.rope_style)
     base = WL.make_fused_inputs(wl)
     x = to_dev_bf16(base.x)
