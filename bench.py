@@ -5,17 +5,19 @@ One step = one pass of the whole hot path over one batch of the workload
 32 heads, bshd):
   1. qnre_forward: fused QKV projection + RMSNorm + RoPE + band scatter of all
      4096 tokens into the 4 ranks' [B, S_global, 8, 128] bands;
-  2. ulysses_pack_head_chunk for each band of the uneven schedule
+  2. the head-chunk pack of every band of the uneven schedule
      [(0,2),(2,4),(6,2)] over H_local = 8, on strided q/k/v views of a
-     [P*B, S_local, 3, 32, 128] projection buffer (all virtual ranks in one call);
-  3. ulysses_merge_output_head_chunk of each packed band's q slice back into a
-     [P*B, S_local, 32, 128] output (pack then merge reproduces q).
+     [P*B, S_local, 3, 32, 128] projection buffer (all virtual ranks, all bands
+     in one ulysses_pack_head_chunk_schedule launch);
+  3. the merge of each packed band's q slice back into a [P*B, S_local, 32, 128]
+     output (one ulysses_merge_output_head_chunk_schedule launch; pack then
+     merge reproduces q).
 Steps 2-3 do not depend on step 1, so they run on a second stream beside it
 (the memory-bound copies fill what the tensor-bound projection leaves idle).
-A copy CTA does not share an SM with a CTA of the persistent fused kernel, so
-the plan leaves --reserve-sms SMs (default 4, one cluster of the fused kernel;
-with the 8 SMs its four-CTA clusters cannot use, the copies get 12) to them:
-qnre_plan_reserve_sms.  --no-overlap runs everything on one stream with every
+A copy CTA does not share an SM with a CTA of the persistent fused kernel; the
+copies run on the 8 SMs its four-CTA clusters cannot use and on SMs as the
+fused kernel's clusters retire.  --reserve-sms N (default 0) leaves N more SMs
+to them: qnre_plan_reserve_sms.  --no-overlap runs everything on one stream with every
 SM given to the fused kernel.
 The L2 (129 MB) is flushed with a 512 MB write between timed steps.
 
@@ -226,12 +228,11 @@ def run_gpu(args):
         if tail is side:
             side.wait_event(start)
         q, k, v = qkv_in[:, :, 0], qkv_in[:, :, 1], qkv_in[:, :, 2]
-        for i, (off, cnt) in enumerate(SCHEDULE):
-            qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, p_[i], stream=tail)
+        qb.ulysses_pack_head_chunk_schedule(q, k, v, W, SCHEDULE, p_, stream=tail)
         if ev:
             ev[2].record(tail)
-        for i, (off, cnt) in enumerate(SCHEDULE):
-            qb.ulysses_merge_output_head_chunk(p_[i][..., :D], W, L, off, m_, stream=tail)
+        qb.ulysses_merge_output_head_chunk_schedule([pk[..., :D] for pk in p_], W, L, [off for off, _ in SCHEDULE],
+                                                    m_, stream=tail)
         if ev:
             ev[3].record(tail)
         if tail is side:
@@ -239,7 +240,7 @@ def run_gpu(args):
         if ev:
             ev[4].record(main)
 
-    launches_per_step = 1 + 2 * len(SCHEDULE)
+    launches_per_step = 3  # fused, pack schedule, merge schedule
     for _ in range(args.warmup):
         step(x, qkv)
         flush.zero_()
@@ -374,9 +375,9 @@ def run_gpu(args):
             "ms_per_step_median": round(statistics.median(step_ms), 5),
             "warm_l2": warm,
             "pack": {"ms": round(statistics.mean(pack_ms), 5), "bytes": pack_bytes, "GB/s": round(pack_gbs, 1),
-                     "frac_hbm": round(pack_gbs / hbm_peak, 4), "launches": len(SCHEDULE)},
+                     "frac_hbm": round(pack_gbs / hbm_peak, 4), "launches": 1, "chunks": len(SCHEDULE)},
             "merge": {"ms": round(statistics.mean(merge_ms), 5), "bytes": merge_bytes, "GB/s": round(merge_gbs, 1),
-                      "frac_hbm": round(merge_gbs / hbm_peak, 4), "launches": len(SCHEDULE)},
+                      "frac_hbm": round(merge_gbs / hbm_peak, 4), "launches": 1, "chunks": len(SCHEDULE)},
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "pipelined: step i's D2H and step i+1's H2D overlap compute; 268 MB of "
@@ -598,6 +599,23 @@ def run_gpu_workload(args):
             if not torch.equal(merged[r], views[r][0]):
                 raise RuntimeError("pack -> merge did not reproduce q")
 
+        # the same schedule through the schedule calls: one launch per rank each
+        def pack_sched():
+            for r, (q, k, v) in enumerate(views):
+                qb.ulysses_pack_head_chunk_schedule(q, k, v, W, wl.schedule, packed[r])
+
+        def merge_sched():
+            for r in range(wl.P):
+                qb.ulysses_merge_output_head_chunk_schedule([pk[..., :D] for pk in packed[r]], W, L,
+                                                            [off for off, _ in wl.schedule], merged[r])
+        for r in range(wl.P):
+            merged[r].zero_()
+        ms_ps, _ = timed(pack_sched)
+        ms_ms, _ = timed(merge_sched)
+        for r in range(wl.P):
+            if not torch.equal(merged[r], views[r][0]):
+                raise RuntimeError("schedule pack -> merge did not reproduce q")
+
         # ordinary and composed exchanges over the same P virtual ranks
         P = wl.P
         ranks = buf.view(P, S, 3, wl.num_heads, D)                 # [P*B, S, 3, H, D] with B = 1
@@ -642,7 +660,11 @@ def run_gpu_workload(args):
         extra_sage = row(ms_sg, n_el * 2 + n_el, 3)   # read bf16 q/k/v once, write 1-byte codes (scales < 0.1 %)
         extra_sage["moved_bytes"] = n_el * 2 + n_el + (2 * n_el // 3) * 2   # + K and V read again by the statistics
         extra_sage["note"] = "GB/s on algorithmic bytes; the statistics pass reads K and V a second time"
-        extra = {"sage2_scatter_qkv": extra_sage,
+        elt_b = 2
+        pk_bytes = sum(2 * wl.B * S * W * cnt * 3 * D * elt_b for _, cnt in wl.schedule) * wl.P
+        mg_bytes = sum(2 * wl.B * S * W * cnt * D * elt_b for _, cnt in wl.schedule) * wl.P
+        extra = {"pack_schedule_call": row(ms_ps, pk_bytes, wl.P), "merge_schedule_call": row(ms_ms, mg_bytes, wl.P),
+                 "sage2_scatter_qkv": extra_sage,
                  "scatter_heads": row(ms_sc, qbytes, 1), "gather_heads": row(ms_ga, qbytes, 1),
                  "scatter_qkv_head_chunk": row(ms_sq, 3 * qbytes, len(wl.schedule)),
                  "gather_output_head_chunk": row(ms_go, qbytes, len(wl.schedule)),
@@ -683,7 +705,7 @@ def main():
                     help="CPU seconds the reference arm spreads over warm-up + timed steps")
     ap.add_argument("--no-overlap", action="store_true",
                     help="run pack/merge after the fused op on one stream instead of beside it")
-    ap.add_argument("--reserve-sms", type=int, default=4,
+    ap.add_argument("--reserve-sms", type=int, default=0,
                     help="SMs the fused kernel leaves to the concurrent pack/merge (overlapped step only)")
     ap.add_argument("--workload", default=None,
                     help="time one row alone on this workload instead of the headline step")

@@ -332,6 +332,34 @@ qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, in
                                               qnre_stream_t stream);
 
 /*
+ * Schedule forms ([PR5027] Description: uneven head schedules; [HC] example
+ * schedule): every chunk of a schedule in one launch, with the same results as
+ * calling the single-chunk function for each chunk in order.
+ *
+ * ulysses_pack_head_chunk_schedule -- chunk i = (head_offsets[i], head_counts[i])
+ *   of the same q, k, v views into outs[i] (as ulysses_pack_head_chunk).
+ *   head_offsets, head_counts, outs   host arrays of num_chunks entries.
+ * ulysses_merge_output_head_chunk_schedule -- chunk i merges received[i] (its own
+ *   head count = shape[2] / world_size) at band head_offsets[i] of the same out
+ *   (as ulysses_merge_output_head_chunk).
+ *   received, head_offsets   host arrays of num_chunks entries; the received views
+ *   share B, S, D and dtype.
+ * Errors: each chunk's checks as in the single-chunk call; num_chunks < 1 or a NULL
+ * array -> QNRE_ERR_INVALID_ARG; num_chunks > 8 -> QNRE_ERR_CAPACITY; pack outputs
+ * that overlap one another -> QNRE_ERR_ALIAS; merge bands that overlap one another
+ * (the chunks run in any order) -> QNRE_ERR_INVALID_ARG.  Chunks whose copies need
+ * different copy units (alignment or innermost strides) are launched one by one.
+ */
+qnre_status_t ulysses_pack_head_chunk_schedule(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                                               const qnre_tensor4_t* v, int world_size, int num_chunks,
+                                               const int* head_offsets, const int* head_counts,
+                                               void* const* outs, qnre_stream_t stream);
+
+qnre_status_t ulysses_merge_output_head_chunk_schedule(const qnre_tensor4_t* const* received, int world_size,
+                                                       int local_heads, int num_chunks, const int* head_offsets,
+                                                       void* out, qnre_stream_t stream);
+
+/*
  * ulysses_scatter_heads -- [ULY] scatter_heads for all P virtual ranks at once:
  * [B, S_local, H, D] per rank -> [B, S_global, H_local, D] per rank, where rank r
  * keeps heads [r*H_local, (r+1)*H_local) of the whole sequence:

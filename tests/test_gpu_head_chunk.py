@@ -141,3 +141,60 @@ def test_pages_headchunk_shape_full_size():
             torch.cuda.synchronize()
             assert np.array_equal(to_host_bits(out), oracle.pack_head_chunk(hq, hk, hv, W, off, cnt))
         assert np.array_equal(to_host_bits(merged), hq)
+
+
+@pytest.mark.parametrize("B,S,H,D,W,sched,tdtype", [
+    (1, 300, 56, 128, 2, [(0, 7), (7, 14), (21, 7)], "bf16"),   # the pages' uneven schedule
+    (2, 130, 12, 128, 3, [(0, 2), (2, 2)], "fp16"),
+    (1, 37, 8, 64, 2, [(0, 1), (1, 2), (3, 1)], "fp32"),
+])
+def test_schedule_calls_match_single_calls(B, S, H, D, W, sched, tdtype):
+    """The schedule forms (one launch each) equal the single-chunk calls made in
+    order, and the oracle, bit for bit."""
+    td = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[tdtype]
+    npd = np.uint32 if tdtype == "fp32" else np.uint16
+    buf = _rand_bits((B, S, 3, H, D), seed=S + W, dtype=npd)
+    tb = _dev(buf, td)
+    q, k, v = tb[:, :, 0], tb[:, :, 1], tb[:, :, 2]
+    L = H // W
+    outs = [torch.empty((B, S, W * cnt, 3 * D), dtype=td, device="cuda") for _, cnt in sched]
+    qb.ulysses_pack_head_chunk_schedule(q, k, v, W, sched, outs)
+    base = _rand_bits((B, S, H, D), seed=3, dtype=npd)
+    merged = _dev(base, td)
+    qb.ulysses_merge_output_head_chunk_schedule([o[..., :D] for o in outs], W, L, [off for off, _ in sched], merged)
+    torch.cuda.synchronize()
+    ref = base.copy()
+    for (off, cnt), o in zip(sched, outs):
+        want = oracle.pack_head_chunk(buf[:, :, 0], buf[:, :, 1], buf[:, :, 2], W, off, cnt)
+        assert np.array_equal(_host(o), want)
+        ref = oracle.merge_output_head_chunk(want[..., :D], W, L, off, ref)
+    assert np.array_equal(_host(merged), ref)
+
+
+def test_schedule_mixed_copy_units_and_rejections():
+    B, S, H, D, W = 1, 40, 8, 128, 2
+    buf = _rand_bits((B, S, 3, H, D), seed=11)
+    tb = to_dev_bf16(buf)
+    q, k, v = tb[:, :, 0], tb[:, :, 1], tb[:, :, 2]
+    sched = [(0, 1), (1, 3)]
+    # the second output starts 2 bytes into a buffer: that chunk takes the element path
+    big = torch.empty((B * S * W * 3 * 3 * D + 8,), dtype=torch.bfloat16, device="cuda")
+    o0 = torch.empty((B, S, W * 1, 3 * D), dtype=torch.bfloat16, device="cuda")
+    o1 = big[1:1 + B * S * W * 3 * 3 * D].view(B, S, W * 3, 3 * D)
+    qb.ulysses_pack_head_chunk_schedule(q, k, v, W, sched, [o0, o1])
+    torch.cuda.synchronize()
+    for (off, cnt), o in zip(sched, [o0, o1]):
+        assert np.array_equal(to_host_bits(o), oracle.pack_head_chunk(buf[:, :, 0], buf[:, :, 1], buf[:, :, 2],
+                                                                      W, off, cnt))
+    out = torch.empty((B, S, W * 2, 3 * D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(qb.QnreError) as e:   # both chunks write the same buffer
+        qb.ulysses_pack_head_chunk_schedule(q, k, v, W, [(0, 2), (2, 2)], [out, out])
+    assert e.value.status == 4
+    with pytest.raises(qb.QnreError) as e:
+        qb.ulysses_pack_head_chunk_schedule(q, k, v, W, [(0, 1)] * 9, [out] * 9)
+    assert e.value.status == 5
+    merged = torch.zeros((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    rec = out[..., :D]
+    with pytest.raises(qb.QnreError) as e:   # bands [0, 2) and [1, 3) overlap
+        qb.ulysses_merge_output_head_chunk_schedule([rec, rec], W, H // W, [0, 1], merged)
+    assert e.value.status == 1

@@ -81,6 +81,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ulysses_pack_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
     lib.ulysses_merge_output_head_chunk.restype = c_int
     lib.ulysses_merge_output_head_chunk.argtypes = [ctypes.POINTER(_Tensor4), c_int, c_int, c_int, c_vp, c_vp]
+    lib.ulysses_pack_head_chunk_schedule.restype = c_int
+    lib.ulysses_pack_head_chunk_schedule.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [
+        c_int, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int), ctypes.POINTER(c_vp), c_vp]
+    lib.ulysses_merge_output_head_chunk_schedule.restype = c_int
+    lib.ulysses_merge_output_head_chunk_schedule.argtypes = [ctypes.POINTER(ctypes.POINTER(_Tensor4)), c_int, c_int,
+                                                            c_int, ctypes.POINTER(c_int), c_vp, c_vp]
     lib.qnre_forward_noalloc.restype = c_int
     lib.qnre_forward_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_int, c_uint, c_int, c_int,
                                          c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, ctypes.POINTER(_Out), c_vp, c_vp]
@@ -228,6 +234,33 @@ def ulysses_merge_output_head_chunk(received, world_size: int, local_heads: int,
     _check(load_library().ulysses_merge_output_head_chunk(ctypes.byref(tr), world_size, local_heads,
                                                           head_offset, out.data_ptr(), _stream_ptr(stream)),
            "ulysses_merge_output_head_chunk")
+    return out
+
+
+def ulysses_pack_head_chunk_schedule(q, k, v, world_size: int, schedule, outs, stream=None):
+    """Every (head_offset, head_count) chunk of `schedule` packed into outs[i] in one launch."""
+    n = len(schedule)
+    tq, tk, tv = _tensor4(q), _tensor4(k), _tensor4(v)
+    offs = (ctypes.c_int * n)(*[int(o) for o, _ in schedule])
+    cnts = (ctypes.c_int * n)(*[int(c) for _, c in schedule])
+    ptrs = (ctypes.c_void_p * n)(*[_contig(o, "pack_head_chunk_schedule") for o in outs])
+    _check(load_library().ulysses_pack_head_chunk_schedule(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                                           world_size, n, offs, cnts, ptrs, _stream_ptr(stream)),
+           "ulysses_pack_head_chunk_schedule")
+    return outs
+
+
+def ulysses_merge_output_head_chunk_schedule(received, world_size: int, local_heads: int, head_offsets, out,
+                                             stream=None):
+    """Every received[i] merged at band head_offsets[i] of `out` in one launch."""
+    n = len(received)
+    views = [_tensor4(r) for r in received]
+    arr = (ctypes.POINTER(_Tensor4) * n)(*[ctypes.pointer(t) for t in views])
+    offs = (ctypes.c_int * n)(*[int(o) for o in head_offsets])
+    _check(load_library().ulysses_merge_output_head_chunk_schedule(arr, world_size, local_heads, n, offs,
+                                                                   _contig(out, "merge_output_head_chunk_schedule"),
+                                                                   _stream_ptr(stream)),
+           "ulysses_merge_output_head_chunk_schedule")
     return out
 
 

@@ -59,13 +59,18 @@ bool dims_ok(std::initializer_list<int64_t> dims) {
   return true;
 }
 
-}  // namespace
+// ---- head-chunk pack and merge, shared by the single-chunk and schedule calls
 
-extern "C" {
+struct PackPlan {
+  LayoutCopyPlan plan{};
+  ByteRange out_range{0, 0};
+  bool same_unit = true;  // one launch covers q, k and v
+  bool empty = false;     // B == 0 or S == 0: nothing to copy
+};
 
-qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const qnre_tensor4_t* v,
-                                      int world_size, int head_offset, int head_count, void* out,
-                                      qnre_stream_t stream) {
+// Validation and copy plan of one pack_ulysses_qkv_head_chunk call.
+qnre_status_t pack_plan(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const qnre_tensor4_t* v, int world_size,
+                        int head_offset, int head_count, void* out, PackPlan* pp) {
   const qnre_tensor4_t* X[3] = {q, k, v};
   ByteRange in[3];
   for (int c = 0; c < 3; ++c) {
@@ -90,10 +95,13 @@ qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor
   const ByteRange o = span(out, static_cast<uint64_t>(B) * S * slots * 3 * D * esz);
   for (int c = 0; c < 3; ++c)
     if (overlaps(o, in[c])) return QNRE_ERR_ALIAS;
-  if (B == 0 || S == 0) return QNRE_OK;  // empty call
+  pp->out_range = o;
+  pp->empty = B == 0 || S == 0;
+  if (pp->empty) return QNRE_OK;
 
   const bool vec = all_vectorisable(X, 3, esz, out);
-  LayoutCopyPlan p{};
+  LayoutCopyPlan& p = pp->plan;
+  p = LayoutCopyPlan{};
   set_sources(p, X, 3, esz, vec);
   for (int c = 0; c < 3; ++c) p.src_rank[c] = H_local * X[c]->stride[2] * esz;
   p.src_head_offset = head_offset;
@@ -111,16 +119,25 @@ qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor
   p.head_count = head_count;
   p.ranks = world_size;
   p.comps = 3;
-  const bool same_unit = vec || (k->stride[3] == q->stride[3] && v->stride[3] == q->stride[3]);
-  if (same_unit) return from_cuda(launch_layout_copy(p, as_stream(stream)));
-  // Element path with different innermost strides: one launch per component.
+  pp->same_unit = vec || (k->stride[3] == q->stride[3] && v->stride[3] == q->stride[3]);
+  return QNRE_OK;
+}
+
+// One pack: a single launch, or (element path with different innermost
+// strides) one launch per component.
+qnre_status_t launch_pack(const PackPlan& pp, const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                          const qnre_tensor4_t* v, void* out, qnre_stream_t stream) {
+  if (pp.same_unit) return from_cuda(launch_layout_copy(pp.plan, as_stream(stream)));
+  const qnre_tensor4_t* X[3] = {q, k, v};
+  const int esz = dtype_size(q->dtype);
+  const int64_t D = q->shape[3];
   for (int c = 0; c < 3; ++c) {
-    LayoutCopyPlan pc = p;
+    LayoutCopyPlan pc = pp.plan;
     pc.src[0] = X[c]->data;
-    pc.src_rank[0] = p.src_rank[c];
-    pc.src_head[0] = p.src_head[c];
-    pc.src_z0[0] = p.src_z0[c];
-    pc.src_s[0] = p.src_s[c];
+    pc.src_rank[0] = pp.plan.src_rank[c];
+    pc.src_head[0] = pp.plan.src_head[c];
+    pc.src_z0[0] = pp.plan.src_z0[c];
+    pc.src_s[0] = pp.plan.src_s[c];
     pc.src_unit = X[c]->stride[3] * esz;
     pc.dst = static_cast<char*>(out) + static_cast<int64_t>(c) * D * esz;
     pc.comps = 1;
@@ -130,8 +147,9 @@ qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor
   return QNRE_OK;
 }
 
-qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size, int local_heads,
-                                              int head_offset, void* out, qnre_stream_t stream) {
+// Validation and copy plan of one merge_ulysses_output_head_chunk call.
+qnre_status_t merge_plan(const qnre_tensor4_t* received, int world_size, int local_heads, int head_offset,
+                         void* out, LayoutCopyPlan* plan, bool* empty) {
   ByteRange in;
   const qnre_status_t st = check_view(received, &in);
   if (st != QNRE_OK) return st;
@@ -145,11 +163,13 @@ qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, in
   if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
   const int64_t out_heads = static_cast<int64_t>(world_size) * local_heads;
   if (overlaps(span(out, static_cast<uint64_t>(B) * S * out_heads * D * esz), in)) return QNRE_ERR_ALIAS;
-  if (B == 0 || S == 0) return QNRE_OK;  // empty call
+  *empty = B == 0 || S == 0;
+  if (*empty) return QNRE_OK;
 
   const qnre_tensor4_t* X[1] = {received};
   const bool vec = all_vectorisable(X, 1, esz, out);
-  LayoutCopyPlan p{};
+  LayoutCopyPlan& p = *plan;
+  p = LayoutCopyPlan{};
   set_sources(p, X, 1, esz, vec);
   p.src_rank[0] = head_count * received->stride[2] * esz;
   p.src_head_offset = 0;
@@ -166,7 +186,91 @@ qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, in
   p.head_count = static_cast<int>(head_count);
   p.ranks = world_size;
   p.comps = 1;
+  return QNRE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qnre_status_t ulysses_pack_head_chunk(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const qnre_tensor4_t* v,
+                                      int world_size, int head_offset, int head_count, void* out,
+                                      qnre_stream_t stream) {
+  PackPlan pp;
+  const qnre_status_t st = pack_plan(q, k, v, world_size, head_offset, head_count, out, &pp);
+  if (st != QNRE_OK || pp.empty) return st;
+  return launch_pack(pp, q, k, v, out, stream);
+}
+
+qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, int world_size, int local_heads,
+                                              int head_offset, void* out, qnre_stream_t stream) {
+  LayoutCopyPlan p{};
+  bool empty = false;
+  const qnre_status_t st = merge_plan(received, world_size, local_heads, head_offset, out, &p, &empty);
+  if (st != QNRE_OK || empty) return st;
   return from_cuda(launch_layout_copy(p, as_stream(stream)));
+}
+
+qnre_status_t ulysses_pack_head_chunk_schedule(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
+                                               const qnre_tensor4_t* v, int world_size, int num_chunks,
+                                               const int* head_offsets, const int* head_counts, void* const* outs,
+                                               qnre_stream_t stream) {
+  if (num_chunks < 1 || head_offsets == nullptr || head_counts == nullptr || outs == nullptr)
+    return QNRE_ERR_INVALID_ARG;
+  if (num_chunks > kLayoutCopyMaxBatch) return QNRE_ERR_CAPACITY;
+  PackPlan pp[kLayoutCopyMaxBatch];
+  bool batch = true;
+  for (int i = 0; i < num_chunks; ++i) {
+    const qnre_status_t st = pack_plan(q, k, v, world_size, head_offsets[i], head_counts[i], outs[i], &pp[i]);
+    if (st != QNRE_OK) return st;
+    batch = batch && pp[i].same_unit && pp[i].plan.unit_bytes == pp[0].plan.unit_bytes;
+  }
+  for (int i = 0; i < num_chunks; ++i)
+    for (int j = i + 1; j < num_chunks; ++j)
+      if (overlaps(pp[i].out_range, pp[j].out_range)) return QNRE_ERR_ALIAS;
+  if (pp[0].empty) return QNRE_OK;  // every chunk shares the views' (B, S)
+  if (batch) {
+    LayoutCopyPlan plans[kLayoutCopyMaxBatch];
+    for (int i = 0; i < num_chunks; ++i) plans[i] = pp[i].plan;
+    return from_cuda(launch_layout_copy_batch(plans, num_chunks, as_stream(stream)));
+  }
+  for (int i = 0; i < num_chunks; ++i) {  // mixed copy units: chunk by chunk
+    const qnre_status_t st = launch_pack(pp[i], q, k, v, outs[i], stream);
+    if (st != QNRE_OK) return st;
+  }
+  return QNRE_OK;
+}
+
+qnre_status_t ulysses_merge_output_head_chunk_schedule(const qnre_tensor4_t* const* received, int world_size,
+                                                       int local_heads, int num_chunks, const int* head_offsets,
+                                                       void* out, qnre_stream_t stream) {
+  if (num_chunks < 1 || received == nullptr || head_offsets == nullptr) return QNRE_ERR_INVALID_ARG;
+  if (num_chunks > kLayoutCopyMaxBatch) return QNRE_ERR_CAPACITY;
+  LayoutCopyPlan plans[kLayoutCopyMaxBatch];
+  int64_t lo[kLayoutCopyMaxBatch], hi[kLayoutCopyMaxBatch];
+  bool empty = false, batch = true;
+  for (int i = 0; i < num_chunks; ++i) {
+    if (received[i] == nullptr) return QNRE_ERR_INVALID_ARG;
+    const qnre_status_t st =
+        merge_plan(received[i], world_size, local_heads, head_offsets[i], out, &plans[i], &empty);
+    if (st != QNRE_OK) return st;
+    for (int d : {0, 1, 3})
+      if (received[i]->shape[d] != received[0]->shape[d]) return QNRE_ERR_INVALID_ARG;
+    if (received[i]->dtype != received[0]->dtype) return QNRE_ERR_INVALID_ARG;
+    lo[i] = head_offsets[i];
+    hi[i] = head_offsets[i] + received[i]->shape[2] / world_size;
+    batch = batch && plans[i].unit_bytes == plans[0].unit_bytes;
+  }
+  for (int i = 0; i < num_chunks; ++i)  // one launch runs the chunks in any order: their bands must be disjoint
+    for (int j = i + 1; j < num_chunks; ++j)
+      if (lo[i] < hi[j] && lo[j] < hi[i]) return QNRE_ERR_INVALID_ARG;
+  if (empty) return QNRE_OK;
+  if (batch) return from_cuda(launch_layout_copy_batch(plans, num_chunks, as_stream(stream)));
+  for (int i = 0; i < num_chunks; ++i) {
+    const cudaError_t e = launch_layout_copy(plans[i], as_stream(stream));
+    if (e != cudaSuccess) return QNRE_ERR_CUDA;
+  }
+  return QNRE_OK;
 }
 
 qnre_status_t ulysses_scatter_heads(const void* x, int P, int B, int S_local, int H, int D, int32_t dtype, void* out,

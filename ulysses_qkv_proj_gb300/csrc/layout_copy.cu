@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kMaxBatch = kLayoutCopyMaxBatch;
 
 struct Args {
   const char* src[3];
@@ -39,10 +40,10 @@ struct Args {
   int head_count, comps, units;
 };
 
+// Rows [blockIdx.y * rows_per_block, +rows_per_block) of one segment.
 template <typename U>
-__global__ void __launch_bounds__(kThreads) layout_copy_kernel(const Args a) {
+__device__ __forceinline__ void copy_block(const Args& a, int seg) {
   // 32-bit index arithmetic (every grid index fits); byte offsets are 64-bit
-  const int seg = blockIdx.x;
   const int slot = seg / a.comps;
   const int c = seg - slot * a.comps;
   const int r = slot / a.head_count;
@@ -93,10 +94,33 @@ __global__ void __launch_bounds__(kThreads) layout_copy_kernel(const Args a) {
   }
 }
 
+template <typename U>
+__global__ void __launch_bounds__(kThreads) layout_copy_kernel(const Args a) {
+  copy_block<U>(a, blockIdx.x);
+}
+
+// Several plans with the same rows and batch extents in one launch: block x
+// runs segment blockIdx.x - first[p] of plan p.
+struct BatchArgs {
+  Args plan[kMaxBatch];
+  int first[kMaxBatch + 1];  // first block of each plan; first[n] = grid x
+  int n;
+};
+
+template <typename U>
+__global__ void __launch_bounds__(kThreads) layout_copy_batch_kernel(const __grid_constant__ BatchArgs b) {
+  const int x = blockIdx.x;
+  int p = 0;
+  while (p + 1 < b.n && x >= b.first[p + 1]) ++p;
+  copy_block<U>(b.plan[p], x - b.first[p]);
+}
+
 }  // namespace
 
-cudaError_t launch_layout_copy(const LayoutCopyPlan& p, cudaStream_t stream) {
-  if (p.S <= 0 || p.Z1 <= 0 || p.Z0 <= 0) return cudaSuccess;
+namespace {
+
+// Kernel arguments of one plan; false when a grid extent is out of range.
+bool make_args(const LayoutCopyPlan& p, Args* out, long long* segments) {
   Args a{};
   for (int c = 0; c < 3; ++c) {
     a.src[c] = static_cast<const char*>(p.src[c]);
@@ -128,16 +152,61 @@ cudaError_t launch_layout_copy(const LayoutCopyPlan& p, cudaStream_t stream) {
   long long rows_per_block = 128;
   while ((p.S + rows_per_block - 1) / rows_per_block > 65535) rows_per_block *= 2;
   a.rows_per_block = static_cast<int>(rows_per_block);
-  const long long segments = static_cast<long long>(p.ranks) * p.head_count * p.comps;
+  *segments = static_cast<long long>(p.ranks) * p.head_count * p.comps;
   const long long zs = p.Z1 * p.Z0;
-  if (segments > 0x7FFFFFFFll || zs > 65535) return cudaErrorInvalidValue;
+  if (*segments > 0x7FFFFFFFll || zs > 65535) return false;
   a.Z0 = static_cast<int>(p.Z0);
-  const dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>((p.S + rows_per_block - 1) / rows_per_block),
-                  static_cast<unsigned>(zs));
+  *out = a;
+  return true;
+}
+
+dim3 rows_grid(const LayoutCopyPlan& p, const Args& a, long long x) {
+  return dim3(static_cast<unsigned>(x), static_cast<unsigned>((p.S + a.rows_per_block - 1) / a.rows_per_block),
+              static_cast<unsigned>(p.Z1 * p.Z0));
+}
+
+}  // namespace
+
+cudaError_t launch_layout_copy(const LayoutCopyPlan& p, cudaStream_t stream) {
+  if (p.S <= 0 || p.Z1 <= 0 || p.Z0 <= 0) return cudaSuccess;
+  Args a;
+  long long segments = 0;
+  if (!make_args(p, &a, &segments)) return cudaErrorInvalidValue;
+  const dim3 grid = rows_grid(p, a, segments);
   switch (p.unit_bytes) {
     case 16: layout_copy_kernel<uint4><<<grid, kThreads, 0, stream>>>(a); break;
     case 4: layout_copy_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(a); break;
     case 2: layout_copy_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStream_t stream) {
+  if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
+  const LayoutCopyPlan& p0 = plans[0];
+  for (int i = 1; i < n; ++i) {
+    if (plans[i].S != p0.S || plans[i].Z1 != p0.Z1 || plans[i].Z0 != p0.Z0 ||
+        plans[i].unit_bytes != p0.unit_bytes)
+      return cudaErrorInvalidValue;
+  }
+  if (p0.S <= 0 || p0.Z1 <= 0 || p0.Z0 <= 0) return cudaSuccess;
+  BatchArgs b{};
+  long long x = 0;
+  for (int i = 0; i < n; ++i) {
+    long long segments = 0;
+    if (!make_args(plans[i], &b.plan[i], &segments)) return cudaErrorInvalidValue;
+    b.first[i] = static_cast<int>(x);
+    x += segments;
+    if (x > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  }
+  b.first[n] = static_cast<int>(x);
+  b.n = n;
+  const dim3 grid = rows_grid(p0, b.plan[0], x);
+  switch (p0.unit_bytes) {
+    case 16: layout_copy_batch_kernel<uint4><<<grid, kThreads, 0, stream>>>(b); break;
+    case 4: layout_copy_batch_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(b); break;
+    case 2: layout_copy_batch_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(b); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

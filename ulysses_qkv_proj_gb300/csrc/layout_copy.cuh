@@ -34,4 +34,9 @@ struct LayoutCopyPlan {
 
 cudaError_t launch_layout_copy(const LayoutCopyPlan& plan, cudaStream_t stream);
 
+// Up to kLayoutCopyMaxBatch plans in one launch: they must share S, Z1, Z0 and
+// unit_bytes, and write disjoint bytes (their blocks run in any order).
+constexpr int kLayoutCopyMaxBatch = 8;
+cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStream_t stream);
+
 }  // namespace qnre
