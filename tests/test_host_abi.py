@@ -223,3 +223,28 @@ def test_sage2_scatter_validation(lib):
 
 def test_plan_reserve_sms_rejects_without_a_plan(lib):
     assert lib.qnre_plan_reserve_sms(None, 8) == 1
+
+
+def test_schedule_calls_reject_before_launch(lib):
+    """Every call here fails a host check, so nothing is launched (fake addresses)."""
+    shp = [1, 8, 4, 128]
+    st = _contig(shp)
+    n = 8 * 4 * 128 * 2
+    q, k, v = (_t4(BASE + i * n, shp, st) for i in range(3))
+    out = BASE + (1 << 20)
+    I2 = ctypes.c_int * 2
+    P2 = ctypes.c_void_p * 2
+    pack = lib.ulysses_pack_head_chunk_schedule
+    args = (ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 2)
+    assert pack(*args, 0, I2(0, 1), I2(1, 1), P2(out, out + n), None) == 1          # no chunks
+    assert pack(*args, 9, (ctypes.c_int * 9)(), (ctypes.c_int * 9)(), (ctypes.c_void_p * 9)(), None) == 5
+    assert pack(*args, 2, None, I2(1, 1), P2(out, out + n), None) == 1              # NULL array
+    assert pack(*args, 2, I2(0, 1), I2(1, 1), P2(out, out + 256), None) == 4        # outputs overlap
+    assert pack(*args, 2, I2(0, 1), I2(1, 2), P2(out, out + n), None) == 1          # chunk 2 past H_local
+    r = _t4(BASE, [1, 8, 2, 128], _contig([1, 8, 2, 128]))
+    merge = lib.ulysses_merge_output_head_chunk_schedule
+    R2 = ctypes.POINTER(qb._Tensor4) * 2
+    views = R2(ctypes.pointer(r), ctypes.pointer(r))
+    assert merge(views, 2, 2, 2, I2(0, 0), out, None) == 1                           # the same band twice
+    assert merge(views, 2, 2, 0, I2(0, 1), out, None) == 1
+    assert merge(None, 2, 2, 2, I2(0, 1), out, None) == 1
