@@ -11,12 +11,17 @@
 //   local head h % H_local, global row r_s * S + s.
 //
 // How (this kernel's design, not the pages'):
-//   * persistent grid of CTA pairs (clusters of 2, one CTA per SM); a pair owns
-//     a 256-token x 256-column tile (= 2 heads), tiles walked in a grouped
-//     raster so concurrent pairs share x and W panels in L2;
+//   * persistent grid of CTA pairs, one CTA per SM; a pair owns a 256-token x
+//     256-column tile (= 2 heads), tiles walked in a grouped raster so
+//     concurrent pairs share x and W panels in L2;
+//   * kPC = 1: clusters of one pair.  kPC = 2: clusters of two pairs on
+//     adjacent row tiles of the same column tile, which need the same W
+//     blocks: pair q loads W block q of each CTA's half once, by TMA multicast
+//     into the matching CTA of both pairs, and a stage is released only when
+//     both pairs' MMAs have committed it;
 //   * warp 0 of each CTA: one thread issues TMA loads of its 128 x-rows
-//     (K-major) and its 128 W-columns (N-major) into a 5-stage ring (128-byte
-//     swizzle); both CTAs' loads complete on the leader CTA's stage barrier;
+//     (K-major) and its W columns (N-major) into a 5-stage ring (128-byte
+//     swizzle); a pair's loads complete on its leader CTA's stage barrier;
 //   * warp 1 of the leader: one thread issues tcgen05.mma.cta_group::2 (M=256,
 //     N=256, K=16, bf16 in, fp32 accumulate in each CTA's tensor memory),
 //     double-buffering the accumulator so the epilogue of tile i overlaps the
