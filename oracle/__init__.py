@@ -12,8 +12,7 @@ Every function is pinned by `tests/test_oracle_pins.py` and
 (closed forms, invariants, brute force on tiny inputs and the hand-written
 fixtures under `tests/golden/`).  `pages_mode.py` is a diagnostic, not a parity
 reference: the pages' own fp32 test-reference form, pinned by
-`tests/test_oracle_pages_mode_pins.py` except for one step (the bf16 cast
-before the norm scale), which is "parity unpinned".
+`tests/test_oracle_pages_mode_pins.py`.  No function is "parity unpinned".
 """
 from .qnre_oracle import *  # noqa: F401,F403
 from .sage2_oracle import *  # noqa: F401,F403

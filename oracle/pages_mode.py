@@ -16,10 +16,10 @@ Readings taken where that sentence leaves a step open:
 
 This module is a diagnostic beside the float64 oracle, which stays the parity
 reference.  Pins: the bf16 rounding against the format's definition (ties to
-even, nearest neighbour, NaN and overflow) and the whole form against the pinned
-float64 oracle within the rounding it adds.  The placement of the cast before the
-scale is "parity unpinned": no input was found on which a pin could tell it from
-a cast after the scale without restating the same steps.
+even, nearest neighbour, NaN and overflow), the whole form against the pinned
+float64 oracle within the rounding it adds, and the cast before the scale on an
+input where the two cast placements give different bf16 results, against the
+steps redone in exact rational arithmetic.
 """
 from __future__ import annotations
 
@@ -48,6 +48,12 @@ def _rms_scale(yg: np.ndarray) -> np.ndarray:
     """1 / sqrt(mean over the head of y^2 + eps), in fp32."""
     ms = np.mean(yg * yg, axis=-1, keepdims=True, dtype=np.float32)
     return (np.float32(1) / np.sqrt(ms + np.float32(RMS_EPS))).astype(np.float32)
+
+
+def _normalise(yg: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """RMSNorm as the pages' reference takes it: the normalised value cast to bf16,
+    then the bf16 weight product, rounded to bf16 again."""
+    return round_bf16(round_bf16(yg * _rms_scale(yg)) * w)
 
 
 def _rope_f32(n: np.ndarray, cs: np.ndarray, rope_style: str) -> np.ndarray:
@@ -81,9 +87,7 @@ def project_norm_rope_pages_mode(x_bits: np.ndarray, w_bits: np.ndarray, q_norm_
     cs = np.asarray(cos_sin, dtype=np.float32)[pos]
     out = np.empty_like(y)
     for g, wbits in ((0, q_norm_w), (1, k_norm_w)):
-        yg = y[:, g]
-        n = round_bf16(yg * _rms_scale(yg))
-        n = round_bf16(n * bf16_to_f64(wbits).astype(np.float32))
+        n = _normalise(y[:, g], bf16_to_f64(wbits).astype(np.float32))
         out[:, g] = round_bf16(_rope_f32(n, cs, rope_style))
     out[:, 2] = round_bf16(y[:, 2])
     return out

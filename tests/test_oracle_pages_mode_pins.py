@@ -1,6 +1,9 @@
 """Pins for the pages' test-reference form (oracle/pages_mode.py, a diagnostic): the
 bf16 rounding against the format's definition, and the whole form against the pinned
 float64 oracle within the error its extra roundings allow.  Planted mistakes trip a pin."""
+from decimal import Decimal, localcontext
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -76,8 +79,59 @@ def check_pages_close_semantics():
     assert PM.pages_close(ref + np.array([0.0101, 0.0201, 0.0401, 1.0101]), ref).tolist() == [False] * 4
 
 
+def _rn(x, bits):
+    """Round a rational to `bits` significant bits, to nearest, ties to even (normal range)."""
+    if x == 0:
+        return Fraction(0)
+    sign = -1 if x < 0 else 1
+    a = abs(Fraction(x))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    scale = Fraction(2) ** (bits - 1 - e)
+    m = a * scale
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * Fraction(fl) / scale
+
+
+def _sqrt_rn(x, bits):
+    """Correctly rounded square root: 80 decimal digits, far more than a 24-bit rounding needs."""
+    with localcontext() as ctx:
+        ctx.prec = 80
+        root = (Decimal(x.numerator) / Decimal(x.denominator)).sqrt()
+    return _rn(Fraction(root), bits)
+
+
+def check_cast_before_scale():
+    """A head of one constant c = 2^-14 with weight 1.125 at position 0 (no rotation):
+    the pages' reference casts the normalised value to bf16 before the scale.  The
+    expected bf16 value is redone here in exact rationals (fp32 = 24 bits, bf16 = 8
+    bits, each operation rounded once); the other cast placement gives another value."""
+    c, w = Fraction(1, 2 ** 14), Fraction(9, 8)
+    eps = Fraction(float(np.float32(PM.RMS_EPS)))
+    r = _rn(1 / _sqrt_rn(_rn(c * c + eps, 24), 24), 24)       # mean of c^2 is exact
+    n = _rn(c * r, 24)
+    want = _rn(_rn(n, 8) * w, 8)
+    other = _rn(_rn(n * w, 24), 8)
+    assert want != other
+    H, D = 1, oracle.HEAD_DIM
+    x = np.zeros((1, H * D), np.uint16)
+    x[0, 0] = 0x3F80                                           # one-hot row: y = W[0, :]
+    wmat = np.zeros((H * D, 3 * H * D), np.uint16)
+    wmat[0, :2 * D] = 0x3880                                   # q and k heads: c = 2^-14
+    wmat[0, 2 * D:] = 0x3F80
+    wn = np.full(D, 0x3F90, np.uint16)                         # 1.125
+    cs = np.zeros((1, D), np.float32)
+    cs[0, :D // 2] = 1.0                                       # position 0: cos 1, sin 0
+    out = PM.project_norm_rope_pages_mode(x, wmat, wn, wn, cs, np.array([0]), H, "interleaved")
+    assert np.all(out[0, :2].astype(np.float64) == float(want))
+
+
 CHECKS = [check_round_bf16_exact_values, check_round_bf16_ties_and_nearest,
-          check_pages_form_within_rounding_of_oracle, check_pages_close_semantics]
+          check_pages_form_within_rounding_of_oracle, check_pages_close_semantics, check_cast_before_scale]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -122,9 +176,13 @@ def _mut_rope_pairing(n, cs, rope_style):      # always rotate-half
     return out
 
 
+def _mut_cast_after_scale(yg, w):               # one rounding after the weight product
+    return PM.round_bf16(yg * PM._rms_scale(yg) * w)
+
+
 @pytest.mark.parametrize("name,mutant", [("round_bf16", _mut_round_truncate), ("round_bf16", _mut_round_ties_up),
                                          ("_rope_f32", _mut_rope_sign), ("_rope_f32", _mut_rope_pairing),
-                                         ("_rms_scale", _mut_rms_sum)])
+                                         ("_rms_scale", _mut_rms_sum), ("_normalise", _mut_cast_after_scale)])
 def test_pages_mode_pins_catch_planted_mistake(name, mutant, monkeypatch):
     monkeypatch.setattr(PM, name, mutant)
     tripped = []
