@@ -27,7 +27,8 @@
  *
  * Conventions for every call:
  *   - Pointers marked "device" point to memory of the current CUDA device; the
- *     caller owns all of it.  No call allocates device memory.
+ *     caller owns all of it.  No call allocates device memory except
+ *     qnre_plan_create (the plan's 16-byte status word).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns without waiting for it.
  *   - Arguments are validated before anything is launched: a call that returns
@@ -151,13 +152,16 @@ qnre_status_t qnre_plan_create(qnre_plan_t* plan, int hidden, int num_heads, int
 qnre_status_t qnre_plan_destroy(qnre_plan_t plan);
 
 /*
- * qnre_plan_reserve_sms -- leave `sms` SMs (rounded up to whole CTA pairs) free
- * of the fused kernel's persistent grid, for work the caller runs beside it on
- * other streams (the pages' producers run "over every SM (no reserved SMs)"
- * only on some architectures: [FUSED] Notes, per-architecture gates).  The
- * fused kernel then runs on the remaining pairs; results are bit-identical for
- * every setting (each tile's arithmetic does not depend on which pair runs it).
- * 0 (the default) uses every SM.  Host-only; applies to later calls of this plan.
+ * qnre_plan_reserve_sms -- leave `sms` SMs free of the fused kernel's
+ * persistent grid, for work the caller runs beside it on other streams (the
+ * pages' producers run "over every SM (no reserved SMs)" only on some
+ * architectures: [FUSED] Notes, per-architecture gates).  The count is rounded
+ * up to whole clusters of the form the call runs: CTA pairs (2 SMs) or two
+ * pairs sharing W (4 SMs; at least one such cluster always remains).  The
+ * fused kernel then runs on the remaining clusters; results are bit-identical
+ * for every setting (each tile's arithmetic does not depend on which cluster
+ * runs it).  0 (the default) uses every SM the clusters can occupy.
+ * Host-only; applies to later calls of this plan.
  * Errors: QNRE_ERR_INVALID_ARG for a NULL plan, sms < 0, or a request that would
  * leave no CTA pair.
  */
@@ -252,7 +256,8 @@ qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, un
  *
  *   hidden, num_heads, P, layout, rope_style, flags
  *             the geometry qnre_plan_create takes (head_dim is 128), with the
- *             same rules and error codes.
+ *             same rules and error codes; flags is 0 or QNRE_FLAG_EPILOGUE_OFF
+ *             (this call always runs the fused kernel one CTA pair per cluster).
  *   B .. out  as in qnre_forward (there is no max_tokens; see the limit below).
  *   device_status_out  device pointer to one unsigned (4-byte aligned), or NULL:
  *             receives this call's QNRE_DEVICE_* bits, in stream order.
