@@ -168,6 +168,28 @@ qnre_status_t qnre_plan_destroy(qnre_plan_t plan);
 qnre_status_t qnre_plan_reserve_sms(qnre_plan_t plan, int sms);
 
 /*
+ * qnre_plan_describe -- how a forward of (B, S_local) with this plan runs (the
+ * pages' sessions report their resolved path and launches per call: [FUSED]
+ * Notes, describe()).  Host-only; no GPU work.  An empty call (B*S_local == 0)
+ * reports zeros.
+ * Errors: QNRE_ERR_INVALID_ARG (NULL plan or info, negative sizes),
+ * QNRE_ERR_CAPACITY (B*S_local > max_tokens).
+ */
+typedef struct {
+  int device;            /* CUDA device the plan is bound to */
+  int pairs_per_cluster; /* 1, or 2: two CTA pairs sharing each W tile by TMA multicast */
+  int clusters;          /* clusters the kernel launches (persistent grid) */
+  int sms;               /* SMs those clusters occupy */
+  int row_tiles;         /* 256-token row tiles of the projection */
+  int col_tiles;         /* 256-column tiles (two heads each) */
+  int work_items;        /* items of the work list (whole tiles or row-tile pairs, and halves) */
+  int half_items;        /* 256 x 128 half items among them (a short last round, small problems) */
+  int launches;          /* kernel launches of one qnre_forward */
+} qnre_plan_info_t;
+
+qnre_status_t qnre_plan_describe(qnre_plan_t plan, int B, int S_local, qnre_plan_info_t* info);
+
+/*
  * qnre_forward -- the fused op on all P virtual ranks at once.  [FUSED], [MATH]:
  *   Y = x W (bf16 operands, fp32 accumulation) with W's columns grouped
  *   Q | K | V (column g*H*128 + h*128 + d);

@@ -345,3 +345,29 @@ def test_w_multicast_bit_identical(S, B, H, P, layout, rope):
         assert np.array_equal(outs[1][g], outs[0][g]), g
     if wl.T <= 1600:
         _full_compare(wl, inp, {g: to_dev_bf16(b) for g, b in outs[1].items()})
+
+
+def test_plan_describe_reports_the_form_that_runs():
+    """qnre_plan_describe agrees with the launch rules: one pair per cluster for an
+    odd handful of row tiles, two pairs sharing W for the benchmarked shape, the
+    flags force either form, and reserved SMs shrink the grid."""
+    tiny = WL.FUSED_WORKLOADS["tiny_p2_s64_h4"]
+    plan = qb.Plan(tiny.hidden, tiny.num_heads, tiny.P, tiny.layout, max_tokens=tiny.B * tiny.S)
+    d = plan.describe(tiny.B, tiny.S)
+    assert d["pairs_per_cluster"] == 1 and d["row_tiles"] == 1 and d["col_tiles"] == 6
+    assert d["half_items"] == d["work_items"] == 12                  # a small problem runs in halves
+    assert plan.describe(0, 0)["clusters"] == 0
+    with pytest.raises(qb.QnreError) as e:
+        plan.describe(tiny.B, tiny.S + 1)
+    assert e.value.status == 5
+    wl = WL.FUSED_WORKLOADS["h4096_p4_s4096"]
+    for flags, ppc in ((0, 2), (qb.FLAG_ONE_PAIR, 1), (qb.FLAG_W_MULTICAST, 2)):
+        p = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, flags=flags)
+        d = p.describe(wl.B, wl.S)
+        assert d["pairs_per_cluster"] == ppc and d["row_tiles"] == 16 and d["col_tiles"] == 48
+        assert d["sms"] == d["clusters"] * 2 * ppc and d["launches"] == 1 and d["clusters"] >= 1
+        full = d["work_items"] - d["half_items"]
+        assert full + d["half_items"] // 2 == (768 if ppc == 1 else 384)   # every tile (or tile pair) once
+        before = d["sms"]
+        p.reserve_sms(16)
+        assert p.describe(wl.B, wl.S)["sms"] <= before - 16

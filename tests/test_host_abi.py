@@ -248,3 +248,8 @@ def test_schedule_calls_reject_before_launch(lib):
     assert merge(views, 2, 2, 2, I2(0, 0), out, None) == 1                           # the same band twice
     assert merge(views, 2, 2, 0, I2(0, 1), out, None) == 1
     assert merge(None, 2, 2, 2, I2(0, 1), out, None) == 1
+
+
+def test_plan_describe_rejects_without_a_plan(lib):
+    info = qb._PlanInfo()
+    assert lib.qnre_plan_describe(None, 1, 1, ctypes.byref(info)) == 1

@@ -47,6 +47,11 @@ class _Out(ctypes.Structure):
                 ("fused", ctypes.c_void_p)]
 
 
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("device", "pairs_per_cluster", "clusters", "sms", "row_tiles",
+                                            "col_tiles", "work_items", "half_items", "launches")]
+
+
 class _Tensor4(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("shape", ctypes.c_int64 * 4),
                 ("stride", ctypes.c_int64 * 4), ("dtype", ctypes.c_int32)]
@@ -72,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qnre_plan_destroy.argtypes = [c_vp]
     lib.qnre_plan_reserve_sms.restype = c_int
     lib.qnre_plan_reserve_sms.argtypes = [c_vp, c_int]
+    lib.qnre_plan_describe.restype = c_int
+    lib.qnre_plan_describe.argtypes = [c_vp, c_int, c_int, ctypes.POINTER(_PlanInfo)]
     lib.qnre_forward.restype = c_int
     lib.qnre_forward.argtypes = [c_vp, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
                                  ctypes.POINTER(_Out), c_vp]
@@ -195,6 +202,13 @@ class Plan:
     def reserve_sms(self, sms: int) -> None:
         """qnre_plan_reserve_sms: leave `sms` SMs free of the fused kernel (0 = use all)."""
         _check(load_library().qnre_plan_reserve_sms(self._handle, sms), "qnre_plan_reserve_sms")
+
+    def describe(self, B: int, S_local: int) -> Dict[str, int]:
+        """qnre_plan_describe: how a forward of (B, S_local) runs (clusters, SMs, work list)."""
+        info = _PlanInfo()
+        _check(load_library().qnre_plan_describe(self._handle, B, S_local, ctypes.byref(info)),
+               "qnre_plan_describe")
+        return {name: getattr(info, name) for name, _ in _PlanInfo._fields_}
 
     def device_status(self, clear: bool = True, stream=None) -> int:
         bits = ctypes.c_uint(0)

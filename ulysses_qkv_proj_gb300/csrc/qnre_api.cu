@@ -176,6 +176,40 @@ qnre_status_t qnre_plan_destroy(qnre_plan_t plan) {
 
 namespace {
 
+// The form a forward takes: clusters of one pair, or of two pairs sharing W
+// through multicast (forced by a flag, else chosen when such clusters fit and
+// the row tiles pair up: an odd last row tile is paired with an empty one, so
+// odd counts take it only when that waste is small), and its work list.
+struct LaunchShape {
+  int pairs_per_cluster;  // 1 or 2
+  int units;              // clusters launched
+  int num_mp_tiles;       // row units of the raster
+  int group_m;            // raster group, in row units
+  int num_full, num_work; // whole items, all items (whole + halves)
+};
+
+LaunchShape launch_shape(const qnre_plan_s* plan, int m_tiles, int n_tiles, int group_m) {
+  LaunchShape ls{};
+  const bool multicast = !(plan->flags & QNRE_FLAG_ONE_PAIR) && plan->max_quads >= 1 &&
+                         ((plan->flags & QNRE_FLAG_W_MULTICAST) || m_tiles % 2 == 0 || m_tiles >= 16);
+  if (multicast) {
+    // work item = (pair of adjacent row tiles, column tile); a short last round
+    // is split into 256 x 128 halves like the one-pair kernel's
+    ls.pairs_per_cluster = 2;
+    ls.num_mp_tiles = (m_tiles + 1) / 2;
+    ls.group_m = std::max(1, (group_m + 1) / 2);
+    qnre::plan_work(ls.num_mp_tiles * n_tiles, plan->max_quads, &ls.num_full, &ls.num_work);
+    ls.units = std::min(ls.num_work, plan->max_quads);
+  } else {
+    ls.pairs_per_cluster = 1;
+    ls.num_mp_tiles = m_tiles;
+    ls.group_m = group_m;
+    qnre::plan_work(m_tiles * n_tiles, plan->max_pairs, &ls.num_full, &ls.num_work);
+    ls.units = std::min(ls.num_work, plan->max_pairs);
+  }
+  return ls;
+}
+
 // The fused forward; `ready` (device [P] words, or null) receives the
 // per-destination publication counts.
 qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, const void* w_qkv,
@@ -278,25 +312,13 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.group_m = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(m_tiles, (static_cast<int64_t>(QNRE_RASTER_L2_MB) << 20) / panel_bytes)));
   a.num_k_blocks = static_cast<int>(K / qnre::kBK);
-  // Clusters of two pairs sharing W through multicast: forced by the flag, else
-  // chosen when they fit and the row tiles pair up (an odd last row tile is
-  // paired with an empty one, so odd counts take it only when that waste is small).
-  const bool multicast =
-      !(plan->flags & QNRE_FLAG_ONE_PAIR) && plan->max_quads >= 1 &&
-      ((plan->flags & QNRE_FLAG_W_MULTICAST) || a.num_m_tiles % 2 == 0 || a.num_m_tiles >= 16);
-  int units = 0;
-  if (multicast) {
-    // work item = (pair of adjacent row tiles, column tile); a short last round
-    // is split into 256 x 128 halves like the one-pair kernel's
-    a.num_mp_tiles = (a.num_m_tiles + 1) / 2;
-    a.group_m = std::max(1, (a.group_m + 1) / 2);
-    qnre::plan_work(a.num_mp_tiles * a.num_n_tiles, plan->max_quads, &a.num_full, &a.num_work);
-    units = std::min(a.num_work, plan->max_quads);
-  } else {
-    a.num_mp_tiles = a.num_m_tiles;
-    qnre::plan_work(a.num_tiles, plan->max_pairs, &a.num_full, &a.num_work);
-    units = std::min(a.num_work, plan->max_pairs);
-  }
+  const LaunchShape ls = launch_shape(plan, a.num_m_tiles, a.num_n_tiles, a.group_m);
+  const bool multicast = ls.pairs_per_cluster == 2;
+  const int units = ls.units;
+  a.num_mp_tiles = ls.num_mp_tiles;
+  a.group_m = ls.group_m;
+  a.num_full = ls.num_full;
+  a.num_work = ls.num_work;
   if (ready != nullptr &&
       cudaMemsetAsync(ready, 0, static_cast<size_t>(P) * 4, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return QNRE_ERR_CUDA;
@@ -321,6 +343,29 @@ qnre_status_t qnre_forward_publish(qnre_plan_t plan, int B, int S_local, const v
   if (ready == nullptr) return QNRE_ERR_INVALID_ARG;
   return forward_impl(plan, B, S_local, x, w_qkv, q_norm_w, k_norm_w, cos_sin, n_pos, positions, out, ready,
                       stream);
+}
+
+qnre_status_t qnre_plan_describe(qnre_plan_t plan, int B, int S_local, qnre_plan_info_t* info) {
+  if (plan == nullptr || info == nullptr || B < 0 || S_local < 0) return QNRE_ERR_INVALID_ARG;
+  const int64_t tokens_per_rank = static_cast<int64_t>(B) * S_local;
+  if (tokens_per_rank > plan->max_tokens) return QNRE_ERR_CAPACITY;
+  qnre_plan_info_t r{};
+  r.device = plan->device;
+  if (tokens_per_rank > 0) {
+    const int64_t T = tokens_per_rank * plan->P;
+    const int64_t N = 3 * static_cast<int64_t>(plan->num_heads) * QNRE_HEAD_DIM;
+    r.row_tiles = static_cast<int>((T + qnre::kPairM - 1) / qnre::kPairM);
+    r.col_tiles = static_cast<int>((N + qnre::kBN - 1) / qnre::kBN);
+    const LaunchShape ls = launch_shape(plan, r.row_tiles, r.col_tiles, 1);
+    r.pairs_per_cluster = ls.pairs_per_cluster;
+    r.clusters = ls.units;
+    r.sms = ls.units * 2 * ls.pairs_per_cluster;
+    r.work_items = ls.num_work;
+    r.half_items = ls.num_work - ls.num_full;
+    r.launches = 1;
+  }
+  *info = r;
+  return QNRE_OK;
 }
 
 qnre_status_t qnre_ready_target(qnre_plan_t plan, int B, int S_local, unsigned* target) {
