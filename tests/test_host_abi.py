@@ -253,3 +253,18 @@ def test_schedule_calls_reject_before_launch(lib):
 def test_plan_describe_rejects_without_a_plan(lib):
     info = qb._PlanInfo()
     assert lib.qnre_plan_describe(None, 1, 1, ctypes.byref(info)) == 1
+
+
+def test_scatter_qkv_alias_covers_every_destination_band(lib):
+    """out [P, B, P*S, head_count, 3D] is P times one source band: an input that
+    overlaps only the last destination rank's part of it is still an alias."""
+    P, PB, S, H, D = 2, 2, 8, 4, 128
+    shp = [PB, S, H, D]
+    n = PB * S * H * D * 2
+    q, k, v = (_t4(BASE + i * n, shp, _contig(shp)) for i in range(3))
+    out_bytes = P * PB * S * 1 * 3 * D * 2
+    out = BASE - out_bytes + 256                 # its last 256 bytes lie over q
+    f = lib.ulysses_scatter_qkv_head_chunk
+    assert f(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), P, 0, 1, out, None) == 4
+    out = BASE - out_bytes // P - 256            # clear of q for one band only
+    assert f(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), P, 0, 1, out, None) == 4

@@ -456,7 +456,8 @@ qnre_status_t ulysses_scatter_qkv_head_chunk(const qnre_tensor4_t* q, const qnre
   if (PB > 65535) return QNRE_ERR_CAPACITY;
   const int esz = dtype_size(q->dtype);
   if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
-  const ByteRange o = span(out, static_cast<uint64_t>(PB) * S * head_count * 3 * D * esz);
+  // out [P, B, P*S, head_count, 3D]: P * PB * S head rows of 3D elements
+  const ByteRange o = span(out, static_cast<uint64_t>(P) * PB * S * head_count * 3 * D * esz);
   for (int c = 0; c < 3; ++c)
     if (overlaps(o, in[c])) return QNRE_ERR_ALIAS;
   if (PB == 0 || S == 0) return QNRE_OK;
