@@ -91,6 +91,8 @@ typedef enum { QNRE_DTYPE_BF16 = 0, QNRE_DTYPE_FP16 = 1, QNRE_DTYPE_FP32 = 2 } q
                                          kernel stopped early and its outputs are incomplete */
 #define QNRE_DEVICE_READY_TIMEOUT 0x4u /* qnre_wait_ready gave up before every readiness word reached
                                           its target */
+#define QNRE_DEVICE_BOUNDS 0x8u /* debug build only (libqnre_debug.so): a computed output row fell
+                                   outside its output tensor and was not stored */
 
 typedef struct qnre_plan_s* qnre_plan_t;
 
@@ -265,6 +267,23 @@ qnre_status_t qnre_wait_ready(qnre_plan_t plan, const unsigned* ready, unsigned 
  * Returns QNRE_ERR_DEVICE when any bit is set, QNRE_OK otherwise. */
 qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, unsigned* bits,
                                       int clear);
+
+/* qnre_debug_bounds -- the debug build's count of skipped accesses.
+ * libqnre_debug.so (the same sources built with QNRE_DEBUG_BOUNDS=1) checks
+ * every load and store of the layout copy kernels and of the Sage2 kernels
+ * against the byte range of the buffer the call was given for it (the same
+ * ranges the alias checks use), and every head-row store of the fused epilogue
+ * against its output tensor.  An access outside its range is not performed:
+ * the layout and Sage2 kernels count it here, the fused kernel raises
+ * QNRE_DEVICE_BOUNDS in the plan's status word.  Nothing traps; the calls'
+ * results are then incomplete, and a correct build never counts anything.
+ *   violations  host, out: accesses skipped since the last reset (all kernels,
+ *               all streams, this device).
+ *   reset       non-zero: set the count to 0 after reading it.
+ * Synchronises the device (a symbol copy).  Errors: QNRE_ERR_INVALID_ARG for a
+ * NULL pointer, QNRE_ERR_UNSUPPORTED in the release build (libqnre.so, which
+ * has no checks), QNRE_ERR_CUDA when the copy fails. */
+qnre_status_t qnre_debug_bounds(unsigned long long* violations, int reset);
 
 /*
  * qnre_forward_noalloc -- qnre_forward without a plan and without any device

@@ -255,6 +255,36 @@ def test_plan_describe_rejects_without_a_plan(lib):
     assert lib.qnre_plan_describe(None, 1, 1, ctypes.byref(info)) == 1
 
 
+def test_debug_bounds_release_build_is_unsupported(lib):
+    n = ctypes.c_ulonglong(7)
+    assert lib.qnre_debug_bounds(ctypes.byref(n), 0) == 2  # QNRE_ERR_UNSUPPORTED: no checks compiled in
+    assert n.value == 0
+    assert lib.qnre_debug_bounds(None, 0) == 1
+
+
+def test_debug_build_exports_every_declared_function():
+    """libqnre_debug.so (QNRE_DEBUG_BOUNDS=1) builds from the same sources and
+    serves the same ABI; without a GPU its count query fails with QNRE_ERR_CUDA."""
+    from ulysses_qkv_proj_gb300 import build
+    path = build.build(debug_bounds=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in qb.header_functions():
+        assert n in exported, n
+    dbg = ctypes.CDLL(path)
+    dbg.qnre_debug_bounds.restype = ctypes.c_int
+    dbg.qnre_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
+    assert dbg.qnre_debug_bounds(None, 0) == 1
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except ImportError:
+        has_gpu = False
+    if not has_gpu:
+        n = ctypes.c_ulonglong(0)
+        assert dbg.qnre_debug_bounds(ctypes.byref(n), 0) == 6
+
+
 def test_scatter_qkv_alias_covers_every_destination_band(lib):
     """out [P, B, P*S, head_count, 3D] is P times one source band: an input that
     overlaps only the last destination rank's part of it is still an alias."""

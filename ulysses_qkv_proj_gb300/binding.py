@@ -18,6 +18,7 @@ from typing import Dict, List, Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqnre.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libqnre_debug.so")  # QNRE_LIB=<this path> selects it
 HEADER = os.path.join(os.path.dirname(HERE), "include", "qnre.h")
 
 QNRE_OK = 0
@@ -33,6 +34,7 @@ FLAG_ONE_PAIR = 0x4
 DEVICE_BAD_POSITION = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 DEVICE_READY_TIMEOUT = 0x4
+DEVICE_BOUNDS = 0x8
 HEAD_DIM = 128
 
 
@@ -60,11 +62,13 @@ class _Tensor4(ctypes.Structure):
 _lib = None
 
 
-def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libqnre.so (built by ulysses_qkv_proj_gb300.build); raises if it is missing."""
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libqnre.so (built by ulysses_qkv_proj_gb300.build), or the library the
+    QNRE_LIB environment variable names (the debug build); raises if it is missing."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("QNRE_LIB") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"libqnre.so not built ({path}); run `python -m ulysses_qkv_proj_gb300.build`")
     lib = ctypes.CDLL(path)
@@ -84,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                  ctypes.POINTER(_Out), c_vp]
     lib.qnre_plan_device_status.restype = c_int
     lib.qnre_plan_device_status.argtypes = [c_vp, c_vp, ctypes.POINTER(c_uint), c_int]
+    lib.qnre_debug_bounds.restype = c_int
+    lib.qnre_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), c_int]
     lib.ulysses_pack_head_chunk.restype = c_int
     lib.ulysses_pack_head_chunk.argtypes = [ctypes.POINTER(_Tensor4)] * 3 + [c_int, c_int, c_int, c_vp, c_vp]
     lib.ulysses_merge_output_head_chunk.restype = c_int
@@ -217,6 +223,16 @@ class Plan:
         if st not in (QNRE_OK, 7):
             raise QnreError(st, "qnre_plan_device_status")
         return bits.value
+
+
+def debug_bounds(reset: bool = True) -> int:
+    """Accesses the debug build's layout and Sage2 kernels skipped (qnre_debug_bounds);
+    raises QnreError(QNRE_ERR_UNSUPPORTED) on the release build."""
+    n = ctypes.c_ulonglong(0)
+    st = load_library().qnre_debug_bounds(ctypes.byref(n), 1 if reset else 0)
+    if st != QNRE_OK:
+        raise QnreError(st, "qnre_debug_bounds")
+    return n.value
 
 
 def qnre_forward(plan: Plan, x, w_qkv, q_norm_w, k_norm_w, cos_sin, positions, out: Dict[str, object],

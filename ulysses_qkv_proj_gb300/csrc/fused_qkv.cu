@@ -349,6 +349,19 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
       }
       uint4* d4 = reinterpret_cast<uint4*>(dst);
       const bool normed = g < 2 && a.epilogue_on;
+#if QNRE_DEBUG_BOUNDS
+      // debug build: a head row outside its output tensor is reported and not stored
+      bool row_ok = valid;
+      if (valid) {
+        const long long off = dst - (a.layout == 0 ? (g == 0 ? a.out_q : (g == 1 ? a.out_k : a.out_v)) : a.out_fused);
+        if (off < 0 || off + 128 > a.out_elems) {
+          atomicOr(a.status, QNRE_DEVICE_BOUNDS);
+          row_ok = false;
+        }
+      }
+#else
+      const bool row_ok = valid;
+#endif
 
       // Pass 1 (q, k): mean square of the head row.
       float scale = 1.0f;
@@ -468,7 +481,7 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
         for (int i = 0; i < 16; ++i) {
           const int src_row = 2 * i + half;
           uint4* rd = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<long long>(d4), src_row));
-          const int rv = __shfl_sync(0xffffffffu, valid ? 1 : 0, src_row);
+          const int rv = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, src_row);
           const uint4 u = stage[src_row * 16 + (chunk ^ (src_row & 15))];
           if (rv) rd[chunk] = u;
         }

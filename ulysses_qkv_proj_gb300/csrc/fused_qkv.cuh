@@ -13,6 +13,10 @@ namespace qnre {
 // (its own A half and its own accumulator rows) and 128 of the columns of the
 // B tile; the pair's tcgen05.mma (cta_group::2) combines them.  A token's whole
 // head row is one TMEM lane of one CTA.
+#ifndef QNRE_DEBUG_BOUNDS
+#define QNRE_DEBUG_BOUNDS 0  // 1: debug build, every output store checked against its buffer's extent
+#endif
+
 constexpr int kBM = 128;                      // rows per CTA (256 per pair)
 constexpr int kPairM = 2 * kBM;
 constexpr int kBN = 256;                      // columns per tile (two heads)
@@ -47,6 +51,7 @@ struct FusedArgs {
   uint16_t* out_fused;
   unsigned* status;
   unsigned* ready;  // per destination rank, or null: per-warp head-row publication counts
+  long long out_elems;  // elements of each output tensor (q, k and v each, or the fused payload)
   long long n_pos;
   int T, K, N, H, H_local, P, B, S;
   int layout;       // 0 bshd, 1 fused

@@ -35,6 +35,17 @@ void set_sources(LayoutCopyPlan& p, const qnre_tensor4_t* const* views, int n, i
   p.src_unit = vec ? 16 : views[0]->stride[3] * esz;
 }
 
+// Byte ranges the debug build checks every access against: the same extents
+// the alias checks use (source c < n, the output).
+void set_ranges(LayoutCopyPlan& p, const ByteRange* in, int n, ByteRange out) {
+  for (int c = 0; c < 3; ++c) {
+    p.src_lo[c] = in[c < n ? c : 0].lo;
+    p.src_hi[c] = in[c < n ? c : 0].hi;
+  }
+  p.dst_lo = out.lo;
+  p.dst_hi = out.hi;
+}
+
 bool all_vectorisable(const qnre_tensor4_t* const* views, int n, int esz, const void* out) {
   if (!aligned(out, 16)) return false;
   for (int c = 0; c < n; ++c)
@@ -119,6 +130,7 @@ qnre_status_t pack_plan(const qnre_tensor4_t* q, const qnre_tensor4_t* k, const 
   p.head_count = head_count;
   p.ranks = world_size;
   p.comps = 3;
+  set_ranges(p, in, 3, o);
   pp->same_unit = vec || (k->stride[3] == q->stride[3] && v->stride[3] == q->stride[3]);
   return QNRE_OK;
 }
@@ -138,6 +150,8 @@ qnre_status_t launch_pack(const PackPlan& pp, const qnre_tensor4_t* q, const qnr
     pc.src_head[0] = pp.plan.src_head[c];
     pc.src_z0[0] = pp.plan.src_z0[c];
     pc.src_s[0] = pp.plan.src_s[c];
+    pc.src_lo[0] = pp.plan.src_lo[c];
+    pc.src_hi[0] = pp.plan.src_hi[c];
     pc.src_unit = X[c]->stride[3] * esz;
     pc.dst = static_cast<char*>(out) + static_cast<int64_t>(c) * D * esz;
     pc.comps = 1;
@@ -162,7 +176,8 @@ qnre_status_t merge_plan(const qnre_tensor4_t* received, int world_size, int loc
   const int esz = dtype_size(received->dtype);
   if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
   const int64_t out_heads = static_cast<int64_t>(world_size) * local_heads;
-  if (overlaps(span(out, static_cast<uint64_t>(B) * S * out_heads * D * esz), in)) return QNRE_ERR_ALIAS;
+  const ByteRange o = span(out, static_cast<uint64_t>(B) * S * out_heads * D * esz);
+  if (overlaps(o, in)) return QNRE_ERR_ALIAS;
   *empty = B == 0 || S == 0;
   if (*empty) return QNRE_OK;
 
@@ -186,6 +201,7 @@ qnre_status_t merge_plan(const qnre_tensor4_t* received, int world_size, int loc
   p.head_count = static_cast<int>(head_count);
   p.ranks = world_size;
   p.comps = 1;
+  set_ranges(p, &in, 1, o);
   return QNRE_OK;
 }
 
@@ -310,6 +326,8 @@ qnre_status_t ulysses_scatter_heads(const void* x, int P, int B, int S_local, in
   p.comps = 1;
   p.unit_bytes = vec ? 16 : esz;
   p.units = static_cast<int>(vec ? D * e / 16 : D);
+  const ByteRange in = span(x, n * esz);
+  set_ranges(p, &in, 1, span(out, n * esz));
   return from_cuda(launch_layout_copy(p, as_stream(stream)));
 }
 
@@ -351,6 +369,8 @@ qnre_status_t ulysses_gather_heads(const void* y, int P, int B, int S_global, in
   p.comps = 1;
   p.unit_bytes = vec ? 16 : esz;
   p.units = static_cast<int>(vec ? D * e / 16 : D);
+  const ByteRange in = span(y, n * esz);
+  set_ranges(p, &in, 1, span(out, n * esz));
   return from_cuda(launch_layout_copy(p, as_stream(stream)));
 }
 
@@ -365,7 +385,8 @@ qnre_status_t ulysses_pack_output_sequence_chunk(const qnre_tensor4_t* x, int wo
   if (B > 65535) return QNRE_ERR_CAPACITY;
   const int esz = dtype_size(x->dtype);
   if (!aligned(out, static_cast<uintptr_t>(esz))) return QNRE_ERR_ALIGNMENT;
-  if (overlaps(span(out, static_cast<uint64_t>(B) * S_g * cnt * D * esz), in)) return QNRE_ERR_ALIAS;
+  const ByteRange o = span(out, static_cast<uint64_t>(B) * S_g * cnt * D * esz);
+  if (overlaps(o, in)) return QNRE_ERR_ALIAS;
   if (B == 0 || S_g == 0) return QNRE_OK;
   const int64_t S = S_g / world_size;
   const qnre_tensor4_t* X[1] = {x};
@@ -385,6 +406,7 @@ qnre_status_t ulysses_pack_output_sequence_chunk(const qnre_tensor4_t* x, int wo
   p.head_count = static_cast<int>(cnt);
   p.ranks = world_size;
   p.comps = 1;
+  set_ranges(p, &in, 1, o);
   return from_cuda(launch_layout_copy(p, as_stream(stream)));
 }
 
@@ -430,6 +452,8 @@ qnre_status_t ulysses_gather_output_head_chunk(const void* x, int P, int B, int 
   p.comps = 1;
   p.unit_bytes = vec ? 16 : esz;
   p.units = static_cast<int>(vec ? D * e / 16 : D);
+  const ByteRange in = span(x, n_in * esz);
+  set_ranges(p, &in, 1, span(out, n_out * esz));
   return from_cuda(launch_layout_copy(p, as_stream(stream)));
 }
 
@@ -484,6 +508,7 @@ qnre_status_t ulysses_scatter_qkv_head_chunk(const qnre_tensor4_t* q, const qnre
   p.head_count = head_count;
   p.ranks = P;
   p.comps = 3;
+  set_ranges(p, in, 3, o);
   const bool same_unit = vec || (k->stride[3] == q->stride[3] && v->stride[3] == q->stride[3]);
   if (same_unit) return from_cuda(launch_layout_copy(p, as_stream(stream)));
   for (int c = 0; c < 3; ++c) {
@@ -494,6 +519,8 @@ qnre_status_t ulysses_scatter_qkv_head_chunk(const qnre_tensor4_t* q, const qnre
     pc.src_z1[0] = p.src_z1[c];
     pc.src_z0[0] = p.src_z0[c];
     pc.src_s[0] = p.src_s[c];
+    pc.src_lo[0] = p.src_lo[c];
+    pc.src_hi[0] = p.src_hi[c];
     pc.src_unit = X[c]->stride[3] * esz;
     pc.dst = static_cast<char*>(out) + static_cast<int64_t>(c) * D * esz;
     pc.comps = 1;

@@ -15,6 +15,8 @@
 // 64-bit.
 #include "layout_copy.cuh"
 
+#include "debug_bounds.cuh"
+
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,7 +40,13 @@ struct Args {
   long long S;
   int rows_per_block;
   int head_count, comps, units;
+#if QNRE_DEBUG_BOUNDS
+  Extent src_ext[3], dst_ext;
+#endif
 };
+
+#define QNRE_SRC_OK(p) QNRE_ACCESS_OK((p), sizeof(U), a.src_ext[c])
+#define QNRE_DST_OK(p) QNRE_ACCESS_OK((p), sizeof(U), a.dst_ext)
 
 // Rows [blockIdx.y * rows_per_block, +rows_per_block) of one segment.
 template <typename U>
@@ -72,15 +80,17 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
     const long long step = rows_per_iter;
     for (long long s = s_begin + lr; s < s_end; s += step * kUnroll) {
       U v[kUnroll];
+      bool ok[kUnroll];
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
-        if (sk < s_end) v[k] = *reinterpret_cast<const U*>(sp + sk * ss);
+        ok[k] = sk < s_end && QNRE_SRC_OK(sp + sk * ss);
+        if (ok[k]) v[k] = *reinterpret_cast<const U*>(sp + sk * ss);
       }
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
-        if (sk < s_end) *reinterpret_cast<U*>(dp + sk * ds) = v[k];
+        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) *reinterpret_cast<U*>(dp + sk * ds) = v[k];
       }
     }
   } else {
@@ -88,8 +98,9 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
     for (long long e = threadIdx.x; e < n; e += kThreads) {
       const long long s = s_begin + e / a.units;
       const long long u = e % a.units;
-      *reinterpret_cast<U*>(dst + s * ds + u * static_cast<long long>(sizeof(U))) =
-          *reinterpret_cast<const U*>(src + s * ss + u * a.src_unit);
+      const char* sp = src + s * ss + u * a.src_unit;
+      char* dp = dst + s * ds + u * static_cast<long long>(sizeof(U));
+      if (QNRE_SRC_OK(sp) && QNRE_DST_OK(dp)) *reinterpret_cast<U*>(dp) = *reinterpret_cast<const U*>(sp);
     }
   }
 }
@@ -144,6 +155,14 @@ bool make_args(const LayoutCopyPlan& p, Args* out, long long* segments) {
   a.head_count = p.head_count;
   a.comps = p.comps;
   a.units = p.units;
+#if QNRE_DEBUG_BOUNDS
+  if (p.dst_hi <= p.dst_lo) return false;  // the debug build checks every plan
+  for (int c = 0; c < p.comps; ++c) {
+    if (p.src_hi[c] <= p.src_lo[c]) return false;
+    a.src_ext[c] = Extent{p.src_lo[c], p.src_hi[c]};
+  }
+  a.dst_ext = output_extent(p.dst_lo, p.dst_hi);
+#endif
 
   // 128 rows per block: on the few SMs that copies get beside the persistent
   // fused kernel, longer blocks amortise each block's start-up (measured: the
@@ -210,6 +229,16 @@ cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStr
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t layout_copy_bounds_violations(unsigned long long* count, bool reset) {
+#if QNRE_DEBUG_BOUNDS
+  return read_bounds_violations(count, reset);
+#else
+  *count = 0;
+  (void)reset;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace qnre

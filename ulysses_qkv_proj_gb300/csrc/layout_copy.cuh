@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace qnre {
 
 // One launch copies head rows of `units` copy units each.  A "segment" is one
@@ -30,6 +32,11 @@ struct LayoutCopyPlan {
   int comps;        // 1 or 3
   int units;        // copy units per head row
   int unit_bytes;   // 16 (vector path), 4 or 2 (element path)
+  // Byte ranges [lo, hi) of each source and of the output, from the entry
+  // point's own extent checks.  The debug build checks every access against
+  // them (and refuses a plan without them); the release build ignores them.
+  uintptr_t src_lo[3], src_hi[3];
+  uintptr_t dst_lo, dst_hi;
 };
 
 cudaError_t launch_layout_copy(const LayoutCopyPlan& plan, cudaStream_t stream);
@@ -38,5 +45,10 @@ cudaError_t launch_layout_copy(const LayoutCopyPlan& plan, cudaStream_t stream);
 // unit_bytes, and write disjoint bytes (their blocks run in any order).
 constexpr int kLayoutCopyMaxBatch = 8;
 cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStream_t stream);
+
+// Debug build: accesses the copy kernels skipped because they fell outside a
+// plan's byte ranges (reset to 0 when `reset`).  Synchronises the device.
+// cudaErrorNotSupported in the release build.
+cudaError_t layout_copy_bounds_violations(unsigned long long* count, bool reset);
 
 }  // namespace qnre

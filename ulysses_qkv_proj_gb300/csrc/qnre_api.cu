@@ -4,6 +4,8 @@
 #include "../../include/qnre.h"
 #include "fused_qkv.cuh"
 #include "api_util.cuh"
+#include "layout_copy.cuh"
+#include "debug_bounds.cuh"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -16,6 +18,10 @@
 #include <cstdint>
 #include <mutex>
 #include <new>
+
+namespace qnre {
+cudaError_t sage2_bounds_violations(unsigned long long* count, bool reset);  // sage2.cu
+}
 
 struct qnre_plan_s {
   int hidden = 0;
@@ -287,6 +293,14 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.out_fused = static_cast<uint16_t*>(bshd ? nullptr : out->fused);
   a.status = plan->d_status;
   a.ready = ready;
+  // [P, B, P*S_local, H_local, D] = T * H * D elements (T = P*B*S_local tokens)
+  a.out_elems = static_cast<long long>(T) * plan->num_heads * (bshd ? 128 : 384);
+#if QNRE_DEBUG_BOUNDS
+  {
+    const long long shrink = static_cast<long long>(qnre::debug_shrink_bytes() / 2);
+    a.out_elems -= shrink < a.out_elems ? shrink : a.out_elems;
+  }
+#endif
   a.n_pos = n_pos;
   a.T = static_cast<int>(T);
   a.K = static_cast<int>(K);
@@ -398,6 +412,22 @@ qnre_status_t qnre_plan_device_status(qnre_plan_t plan, qnre_stream_t stream, un
   if (clear && cudaMemset(plan->d_status, 0, sizeof(unsigned)) != cudaSuccess) return QNRE_ERR_CUDA;
   *bits = host;
   return host ? QNRE_ERR_DEVICE : QNRE_OK;
+}
+
+qnre_status_t qnre_debug_bounds(unsigned long long* violations, int reset) {
+  if (violations == nullptr) return QNRE_ERR_INVALID_ARG;
+  *violations = 0;
+#if QNRE_DEBUG_BOUNDS
+  unsigned long long copies = 0, sage2 = 0;
+  if (qnre::layout_copy_bounds_violations(&copies, reset != 0) != cudaSuccess ||
+      qnre::sage2_bounds_violations(&sage2, reset != 0) != cudaSuccess)
+    return QNRE_ERR_CUDA;
+  *violations = copies + sage2;
+  return QNRE_OK;
+#else
+  (void)reset;
+  return QNRE_ERR_UNSUPPORTED;
+#endif
 }
 
 // --------------------------------------------------------------------------

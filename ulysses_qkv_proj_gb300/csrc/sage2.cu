@@ -27,6 +27,7 @@
 // operation in a fixed order, so the codes are reproducible bit for bit.
 #include "../../include/qnre.h"
 #include "api_util.cuh"
+#include "debug_bounds.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,6 +45,7 @@
 namespace {
 
 using namespace qnre::api;
+using qnre::Extent;
 
 constexpr int kChunk = 256;  // rows per statistics chunk
 constexpr int kQGroup = 32;
@@ -131,6 +133,9 @@ struct StatsArgs {
   float* ksum;  // [P, chunks, B, H, D]
   float* vmax;  // [P, chunks, B, H, D]: max |V| over the chunk's rows below U
   int P, B, L, H, D, chunks, U;
+#if QNRE_DEBUG_BOUNDS
+  Extent k_ext, v_ext, ws_ext;
+#endif
 };
 
 // One CTA: one 256-row chunk of one source rank, 256 / (D / 8) heads.  Thread t
@@ -161,8 +166,10 @@ __global__ void __launch_bounds__(256, 2) stats_partial_kernel(const StatsArgs a
     uint4 kw[kStatsRows], vw[kStatsRows];
 #pragma unroll
     for (int u = 0; u < kStatsRows; ++u) {
-      kw[u] = *reinterpret_cast<const uint4*>(kp + static_cast<long long>(l + u) * a.k.ss);
-      vw[u] = *reinterpret_cast<const uint4*>(vp + static_cast<long long>(l + u) * a.v.ss);
+      const char* ku = kp + static_cast<long long>(l + u) * a.k.ss;
+      const char* vu = vp + static_cast<long long>(l + u) * a.v.ss;
+      kw[u] = QNRE_ACCESS_OK(ku, 16, a.k_ext) ? *reinterpret_cast<const uint4*>(ku) : make_uint4(0, 0, 0, 0);
+      vw[u] = QNRE_ACCESS_OK(vu, 16, a.v_ext) ? *reinterpret_cast<const uint4*>(vu) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kStatsRows; ++u) {
@@ -174,8 +181,10 @@ __global__ void __launch_bounds__(256, 2) stats_partial_kernel(const StatsArgs a
     }
   }
   for (; l < l1; ++l) {
-    const uint4 kw = *reinterpret_cast<const uint4*>(kp + static_cast<long long>(l) * a.k.ss);
-    const uint4 vw = *reinterpret_cast<const uint4*>(vp + static_cast<long long>(l) * a.v.ss);
+    const char* ku = kp + static_cast<long long>(l) * a.k.ss;
+    const char* vu = vp + static_cast<long long>(l) * a.v.ss;
+    const uint4 kw = QNRE_ACCESS_OK(ku, 16, a.k_ext) ? *reinterpret_cast<const uint4*>(ku) : make_uint4(0, 0, 0, 0);
+    const uint4 vw = QNRE_ACCESS_OK(vu, 16, a.v_ext) ? *reinterpret_cast<const uint4*>(vu) : make_uint4(0, 0, 0, 0);
     float f[8];
     unpack8<BF16>(kw, f);
 #pragma unroll
@@ -185,6 +194,7 @@ __global__ void __launch_bounds__(256, 2) stats_partial_kernel(const StatsArgs a
   float vf[8];
   unpack8<BF16>(vm, vf);
   const long long o = ((((static_cast<long long>(r_s) * a.chunks + chunk) * a.B + b) * a.H + h) * a.D) + c0;
+  if (!QNRE_ACCESS_OK(a.ksum + o, 32, a.ws_ext) || !QNRE_ACCESS_OK(a.vmax + o, 32, a.ws_ext)) return;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     a.ksum[o + i] = acc[i];
@@ -202,6 +212,9 @@ struct FinalArgs {
   float* vinv;     // [B, H, D]: 448 / max |V| (0 where the max is 0)
   float* v_scale;  // [P, B, H_l, D]
   int P, B, H, H_l, D, chunks, U;
+#if QNRE_DEBUG_BOUNDS
+  Extent ws_ext, v_scale_ext;
+#endif
 };
 
 __global__ void __launch_bounds__(32) stats_final_kernel(const FinalArgs a) {
@@ -235,10 +248,11 @@ __global__ void __launch_bounds__(32) stats_final_kernel(const FinalArgs a) {
     total = __fadd_rn(total, rank_sum);
   }
   const long long o = (static_cast<long long>(b) * a.H + h) * a.D + d;
-  a.kmean[o] = __fdiv_rn(total, static_cast<float>(a.U));
-  a.vinv[o] = reciprocal(vm, 448.0f);
+  if (QNRE_ACCESS_OK(a.kmean + o, 4, a.ws_ext)) a.kmean[o] = __fdiv_rn(total, static_cast<float>(a.U));
+  if (QNRE_ACCESS_OK(a.vinv + o, 4, a.ws_ext)) a.vinv[o] = reciprocal(vm, 448.0f);
   const int r = h / a.H_l, hl = h - r * a.H_l;
-  a.v_scale[((static_cast<long long>(r) * a.B + b) * a.H_l + hl) * a.D + d] = __fdiv_rn(vm, 448.0f);
+  float* vs = a.v_scale + ((static_cast<long long>(r) * a.B + b) * a.H_l + hl) * a.D + d;
+  if (QNRE_ACCESS_OK(vs, 4, a.v_scale_ext)) *vs = __fdiv_rn(vm, 448.0f);
 }
 
 // ---------------------------------------------------------------------------
@@ -254,6 +268,10 @@ struct QuantArgs {
   float* q_scale;  // [P, B, H_l, wq]
   float* k_scale;  // [P, B, H_l, wk]
   int P, B, L, H, H_l, D, S, S_pad, U, wq, wk;
+#if QNRE_DEBUG_BOUNDS
+  Extent src_ext[3];  // v, q, k (landing order)
+  Extent q_out_ext, k_out_ext, v_out_ext, q_scale_ext, k_scale_ext;
+#endif
 };
 
 // Max over the CTA's 256 threads (holds two barriers).
@@ -358,8 +376,9 @@ __global__ void __launch_bounds__(256, QNRE_SAGE2_QUANT_MIN_BLOCKS) quantize_ker
       const char* base = t.data + h * t.sh + c0 * 2;
 #pragma unroll
       for (int u = 0; u < RPT; ++u) {
-        if (u < n_live)
-          cp_async16(&slot(c, u), base + static_cast<long long>(zr[u]) * t.sz + static_cast<long long>(lr[u]) * t.ss);
+        const char* gp = base + static_cast<long long>(zr[u]) * t.sz + static_cast<long long>(lr[u]) * t.ss;
+        if (u < n_live && QNRE_ACCESS_OK(gp, 16, a.src_ext[c]))
+          cp_async16(&slot(c, u), gp);
         else
           slot(c, u) = make_uint4(0, 0, 0, 0);  // a dead row reads as +0
       }
@@ -419,18 +438,20 @@ __global__ void __launch_bounds__(256, QNRE_SAGE2_QUANT_MIN_BLOCKS) quantize_ker
     }
     if (tid == 0) {
       const int gq = 2 * g;
-      if (gq < a.wq) a.q_scale[sc_base * a.wq + gq] = __fdiv_rn(m0, 127.0f);
-      if (gq + 1 < a.wq) a.q_scale[sc_base * a.wq + gq + 1] = __fdiv_rn(m1, 127.0f);
+      float* qs = a.q_scale + sc_base * a.wq + gq;
+      if (gq < a.wq && QNRE_ACCESS_OK(qs, 4, a.q_scale_ext)) qs[0] = __fdiv_rn(m0, 127.0f);
+      if (gq + 1 < a.wq && QNRE_ACCESS_OK(qs + 1, 4, a.q_scale_ext)) qs[1] = __fdiv_rn(m1, 127.0f);
     }
 #pragma unroll
     for (int u = 0; u < RPT; ++u) {
-      if (sr + u < a.S) {
+      int8_t* qd = a.q_out + out0 + u * row_step;
+      if (sr + u < a.S && QNRE_ACCESS_OK(qd, 8, a.q_out_ext)) {
         float f[8];
         unpack8<BF16>(slot(1, u), f);  // dead rows are +0 and encode as 0
         uint32_t t[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = int8_bits(f[i], inv);
-        *reinterpret_cast<uint2*>(a.q_out + out0 + u * row_step) =
+        *reinterpret_cast<uint2*>(qd) =
             make_uint2(pack_low_bytes(t[0], t[1], t[2], t[3]), pack_low_bytes(t[4], t[5], t[6], t[7]));
       }
     }
@@ -462,18 +483,20 @@ __global__ void __launch_bounds__(256, QNRE_SAGE2_QUANT_MIN_BLOCKS) quantize_ker
     }
     const float m = block_max(xmax, red);
     const float inv = reciprocal(m, 127.0f);
-    if (tid == 0 && g < a.wk) a.k_scale[sc_base * a.wk + g] = __fdiv_rn(m, 127.0f);
+    float* ks = a.k_scale + sc_base * a.wk + g;
+    if (tid == 0 && g < a.wk && QNRE_ACCESS_OK(ks, 4, a.k_scale_ext)) *ks = __fdiv_rn(m, 127.0f);
     // the transposed V codes are complete (block_max's barriers): 16-byte stores
     for (int idx = tid; idx < a.D * 4; idx += 256) {
       const int c = idx >> 2, part = idx & 3;
       const uint32_t* row = vt + c * kVRowWords + part * 4;
       uint8_t* dst = a.v_out + (((static_cast<long long>(r) * a.B + b) * a.D + c) * a.H_l + hl) * a.S_pad + s0 +
                      part * 16;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
+      if (QNRE_ACCESS_OK(dst, 16, a.v_out_ext)) *reinterpret_cast<uint4*>(dst) = make_uint4(row[0], row[1], row[2], row[3]);
     }
 #pragma unroll
     for (int u = 0; u < RPT; ++u) {
-      if (sr + u < a.S) {
+      int8_t* kd = a.k_out + out0 + u * row_step;
+      if (sr + u < a.S && QNRE_ACCESS_OK(kd, 8, a.k_out_ext)) {
         uint2 code = make_uint2(0, 0);  // rows at or past U are code 0
         if (u < n_live) {
           float f[8];
@@ -483,7 +506,7 @@ __global__ void __launch_bounds__(256, QNRE_SAGE2_QUANT_MIN_BLOCKS) quantize_ker
           for (int i = 0; i < 8; ++i) t[i] = int8_bits(__fsub_rn(f[i], mean[i]), inv);
           code = make_uint2(pack_low_bytes(t[0], t[1], t[2], t[3]), pack_low_bytes(t[4], t[5], t[6], t[7]));
         }
-        *reinterpret_cast<uint2*>(a.k_out + out0 + u * row_step) = code;
+        *reinterpret_cast<uint2*>(kd) = code;
       }
     }
   }
@@ -620,6 +643,11 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
   sa.D = g.D;
   sa.chunks = g.chunks;
   sa.U = g.U;
+#if QNRE_DEBUG_BOUNDS
+  sa.k_ext = Extent{in[1].lo, in[1].hi};
+  sa.v_ext = Extent{in[2].lo, in[2].hi};
+  sa.ws_ext = Extent{outs[6].lo, outs[6].hi};
+#endif
   const int heads_per_cta = 256 / (g.D / 8);
   const dim3 sgrid((g.H + heads_per_cta - 1) / heads_per_cta, g.chunks, P * g.B);
   if (bf16) stats_partial_kernel<true><<<sgrid, 256, 0, s>>>(sa);
@@ -639,6 +667,10 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
   fa.D = g.D;
   fa.chunks = g.chunks;
   fa.U = g.U;
+#if QNRE_DEBUG_BOUNDS
+  fa.ws_ext = Extent{outs[6].lo, outs[6].hi};
+  fa.v_scale_ext = Extent{outs[5].lo, outs[5].hi};
+#endif
   stats_final_kernel<<<dim3(g.H, g.B, g.D / 32), 32, 0, s>>>(fa);
   if (cudaGetLastError() != cudaSuccess) return QNRE_ERR_CUDA;
 
@@ -664,6 +696,16 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
   qa.U = g.U;
   qa.wq = g.wq;
   qa.wk = g.wk;
+#if QNRE_DEBUG_BOUNDS
+  qa.src_ext[0] = Extent{in[2].lo, in[2].hi};
+  qa.src_ext[1] = Extent{in[0].lo, in[0].hi};
+  qa.src_ext[2] = Extent{in[1].lo, in[1].hi};
+  qa.q_out_ext = qnre::output_extent(outs[0].lo, outs[0].hi);
+  qa.k_out_ext = qnre::output_extent(outs[1].lo, outs[1].hi);
+  qa.v_out_ext = qnre::output_extent(outs[2].lo, outs[2].hi);
+  qa.q_scale_ext = Extent{outs[3].lo, outs[3].hi};
+  qa.k_scale_ext = Extent{outs[4].lo, outs[4].hi};
+#endif
   const dim3 qgrid(g.H, g.S_pad / kKGroup, g.B);
   if (g.D == 128 && bf16) quantize_kernel<4, true><<<qgrid, 256, quantize_smem_bytes<4>(), s>>>(qa);
   else if (g.D == 128) quantize_kernel<4, false><<<qgrid, 256, quantize_smem_bytes<4>(), s>>>(qa);
@@ -673,3 +715,17 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
 }
 
 }  // extern "C"
+
+namespace qnre {
+
+cudaError_t sage2_bounds_violations(unsigned long long* count, bool reset) {
+#if QNRE_DEBUG_BOUNDS
+  return read_bounds_violations(count, reset);
+#else
+  *count = 0;
+  (void)reset;
+  return cudaErrorNotSupported;
+#endif
+}
+
+}  // namespace qnre
