@@ -12,7 +12,9 @@
 // vectors (when rows are 16-byte aligned with unit innermost stride) at a fixed
 // column of the segment while it walks the rows, so all index arithmetic is
 // hoisted out of the loop; four rows are in flight per thread.  Offsets are
-// 64-bit.
+// 64-bit.  Loads and stores are cache-streaming (ld/st .cs): every copied byte
+// is touched once, so its lines are the first to leave L2, and a tensor-core
+// kernel running beside the copy keeps more of its operands there.
 #include "layout_copy.cuh"
 
 #include "debug_bounds.cuh"
@@ -85,12 +87,12 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
         ok[k] = sk < s_end && QNRE_SRC_OK(sp + sk * ss);
-        if (ok[k]) v[k] = *reinterpret_cast<const U*>(sp + sk * ss);
+        if (ok[k]) v[k] = __ldcs(reinterpret_cast<const U*>(sp + sk * ss));
       }
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
-        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) *reinterpret_cast<U*>(dp + sk * ds) = v[k];
+        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) __stcs(reinterpret_cast<U*>(dp + sk * ds), v[k]);
       }
     }
   } else {
@@ -100,7 +102,7 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
       const long long u = e % a.units;
       const char* sp = src + s * ss + u * a.src_unit;
       char* dp = dst + s * ds + u * static_cast<long long>(sizeof(U));
-      if (QNRE_SRC_OK(sp) && QNRE_DST_OK(dp)) *reinterpret_cast<U*>(dp) = *reinterpret_cast<const U*>(sp);
+      if (QNRE_SRC_OK(sp) && QNRE_DST_OK(dp)) __stcs(reinterpret_cast<U*>(dp), __ldcs(reinterpret_cast<const U*>(sp)));
     }
   }
 }
