@@ -162,7 +162,11 @@ qnre_status_t qnre_plan_destroy(qnre_plan_t plan);
  * pairs sharing W (4 SMs; at least one such cluster always remains).  The
  * fused kernel then runs on the remaining clusters; results are bit-identical
  * for every setting (each tile's arithmetic does not depend on which cluster
- * runs it).  0 (the default) uses every SM the clusters can occupy.
+ * runs it).  0 (the default) reserves nothing.  In either case a forward
+ * launches the fewest of the clusters it may use that finish its work list in
+ * as many rounds as all of them would (qnre_plan_describe reports the count):
+ * the clusters that would only idle through the last round are left to other
+ * streams.
  * Host-only; applies to later calls of this plan.
  * Errors: QNRE_ERR_INVALID_ARG for a NULL plan, sms < 0, or a request that would
  * leave no CTA pair.
@@ -180,7 +184,8 @@ qnre_status_t qnre_plan_reserve_sms(qnre_plan_t plan, int sms);
 typedef struct {
   int device;            /* CUDA device the plan is bound to */
   int pairs_per_cluster; /* 1, or 2: two CTA pairs sharing each W tile by TMA multicast */
-  int clusters;          /* clusters the kernel launches (persistent grid) */
+  int clusters;          /* clusters the kernel launches (persistent grid): the fewest of
+                            those available that finish in as many rounds as all of them */
   int sms;               /* SMs those clusters occupy */
   int row_tiles;         /* 256-token row tiles of the projection */
   int col_tiles;         /* 256-column tiles (two heads each) */

@@ -368,6 +368,45 @@ def test_plan_describe_reports_the_form_that_runs():
         assert d["sms"] == d["clusters"] * 2 * ppc and d["launches"] == 1 and d["clusters"] >= 1
         full = d["work_items"] - d["half_items"]
         assert full + d["half_items"] // 2 == (768 if ppc == 1 else 384)   # every tile (or tile pair) once
-        before = d["sms"]
+        total = torch.cuda.get_device_properties(0).multi_processor_count
         p.reserve_sms(16)
-        assert p.describe(wl.B, wl.S)["sms"] <= before - 16
+        assert p.describe(wl.B, wl.S)["sms"] <= total - 16
+
+
+def _plan_work(tiles, units):
+    """The work list's split rule (whole tiles, and a short last round in halves)."""
+    if 2 * tiles <= units:
+        return 0, 2 * tiles
+    rem = tiles % units
+    if rem > 0 and 2 * rem <= units:
+        return tiles - rem, tiles + rem
+    return tiles, tiles
+
+
+def _makespan_halves(full, work, units):
+    loads = [0] * units
+    for w in range(work):
+        loads[w % units] += 2 if w < full else 1
+    return max(loads)
+
+
+@pytest.mark.parametrize("flags", [0, qb.FLAG_ONE_PAIR])
+def test_fewest_clusters_for_the_same_makespan(flags):
+    """A forward launches the fewest clusters that finish in as many rounds as one
+    cluster fewer could not: for the 4096-token shape the last round would leave
+    clusters idle, and those are not launched."""
+    wl = WL.FUSED_WORKLOADS["h4096_p4_s4096"]
+    p = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, flags=flags)
+    d = p.describe(wl.B, wl.S)
+    c = d["clusters"]
+    tiles = 384 if d["pairs_per_cluster"] == 2 else 768
+    full, work = d["work_items"] - d["half_items"], d["work_items"]
+    assert (full, work) == _plan_work(tiles, c) or c == work
+    span = _makespan_halves(full, work, c)
+    for fewer in range(1, c):
+        f, w = _plan_work(tiles, fewer)
+        assert _makespan_halves(f, w, min(w, fewer)) > span, fewer
+    per_cluster = 2 * d["pairs_per_cluster"]
+    sm_count = torch.cuda.get_device_properties(0).multi_processor_count
+    assert c * per_cluster <= sm_count
+

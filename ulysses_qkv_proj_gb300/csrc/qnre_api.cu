@@ -194,6 +194,35 @@ struct LaunchShape {
   int num_full, num_work; // whole items, all items (whole + halves)
 };
 
+// Longest load of any unit, in half tiles, when `units` units take the work
+// list of qnre::plan_work round robin (unit u: items u, u + units, ...; items
+// below num_full are whole tiles, the rest halves).  A unit's load is its whole
+// tiles plus its items, and unit 0 has the most of both.
+int makespan_halves(int num_full, int num_work, int units) {
+  return (num_full + units - 1) / units + (num_work + units - 1) / units;
+}
+
+// The fewest units (<= max_units) whose work list finishes in as many half-tile
+// rounds as max_units would: the SMs this leaves idle stay with kernels on
+// other streams (the head-chunk copies beside the projection) at no cost to
+// the projection.
+int fewest_units(int num_tiles, int max_units, int* num_full, int* num_work) {
+  qnre::plan_work(num_tiles, max_units, num_full, num_work);
+  int best = std::min(*num_work, max_units);
+  const int target = makespan_halves(*num_full, *num_work, best);
+  for (int c = best - 1; c >= 1 && static_cast<long long>(c) * target >= 2LL * num_tiles; --c) {
+    int nf = 0, nw = 0;
+    qnre::plan_work(num_tiles, c, &nf, &nw);
+    const int u = std::min(nw, c);
+    if (makespan_halves(nf, nw, u) <= target) {
+      best = u;
+      *num_full = nf;
+      *num_work = nw;
+    }
+  }
+  return best;
+}
+
 LaunchShape launch_shape(const qnre_plan_s* plan, int m_tiles, int n_tiles, int group_m) {
   LaunchShape ls{};
   const bool multicast = !(plan->flags & QNRE_FLAG_ONE_PAIR) && plan->max_quads >= 1 &&
@@ -204,14 +233,12 @@ LaunchShape launch_shape(const qnre_plan_s* plan, int m_tiles, int n_tiles, int 
     ls.pairs_per_cluster = 2;
     ls.num_mp_tiles = (m_tiles + 1) / 2;
     ls.group_m = std::max(1, (group_m + 1) / 2);
-    qnre::plan_work(ls.num_mp_tiles * n_tiles, plan->max_quads, &ls.num_full, &ls.num_work);
-    ls.units = std::min(ls.num_work, plan->max_quads);
+    ls.units = fewest_units(ls.num_mp_tiles * n_tiles, plan->max_quads, &ls.num_full, &ls.num_work);
   } else {
     ls.pairs_per_cluster = 1;
     ls.num_mp_tiles = m_tiles;
     ls.group_m = group_m;
-    qnre::plan_work(m_tiles * n_tiles, plan->max_pairs, &ls.num_full, &ls.num_work);
-    ls.units = std::min(ls.num_work, plan->max_pairs);
+    ls.units = fewest_units(m_tiles * n_tiles, plan->max_pairs, &ls.num_full, &ls.num_work);
   }
   return ls;
 }
