@@ -14,9 +14,11 @@ One step = one pass of the whole hot path over one batch of the workload
      merge reproduces q).
 Steps 2-3 do not depend on step 1, so they run on a second stream beside it
 (the memory-bound copies fill what the tensor-bound projection leaves idle).
-A copy CTA does not share an SM with a CTA of the persistent fused kernel; the
-copies run on the 8 SMs its four-CTA clusters cannot use and on SMs as the
-fused kernel's clusters retire.  --reserve-sms N (default 0) leaves N more SMs
+A copy CTA does not share an SM with a CTA of the persistent fused kernel
+(%smid stamps: none of a step's 4096 copy blocks started beside one); the
+copies run on the SMs its four-CTA clusters leave (12 here: the plan launches
+35 clusters, as many rounds as 36) and on SMs as the fused kernel's clusters
+retire.  --reserve-sms N (default 0) leaves N more SMs
 to them: qnre_plan_reserve_sms.  --no-overlap runs everything on one stream with every
 SM given to the fused kernel.
 The L2 (129 MB) is flushed with a 512 MB write between timed steps.
