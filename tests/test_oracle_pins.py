@@ -569,6 +569,29 @@ def _mut_scatter_heads_swapped(x):
     return out
 
 
+def _mut_scatter_qkv_reversed_sources(q_ranks, k_ranks, v_ranks, head_offset, head_count):
+    # the received blocks stacked in reverse source-rank order along the sequence
+    P = len(q_ranks)
+    packed = [Q.pack_head_chunk(q_ranks[r], k_ranks[r], v_ranks[r], P, head_offset, head_count) for r in range(P)]
+    sent = [[packed[r][:, :, r2 * head_count:(r2 + 1) * head_count, :] for r2 in range(P)] for r in range(P)]
+    received = Q.all_to_all(sent)
+    return [np.concatenate(received[r2][::-1], axis=1) for r2 in range(P)]
+
+
+def _mut_gather_output_slot_order(x_ranks, local_heads, head_offset, out_ranks):
+    # received slots read head-major (j * P + src) instead of source-major
+    P = len(x_ranks)
+    staged = [Q.pack_output_sequence_chunk(x, P) for x in x_ranks]
+    received = Q.all_to_all([[staged[r][r2] for r2 in range(P)] for r in range(P)])
+    res = []
+    for r2 in range(P):
+        band = np.stack(received[r2], axis=0)
+        _, B, S, cnt, D = band.shape
+        rec = band.transpose(1, 2, 3, 0, 4).reshape(B, S, P * cnt, D)
+        res.append(Q.merge_output_head_chunk(rec, P, local_heads, head_offset, out_ranks[r2]))
+    return res
+
+
 MUTANTS = [
     ("qkv_projection", _mut_projection_transposed),
     ("rms_norm", _mut_rms_no_eps),
@@ -586,6 +609,8 @@ MUTANTS = [
     ("pack_output_sequence_chunk", _mut_seqchunk_wrong_rows),
     ("all_to_all", _mut_all_to_all_identity),
     ("scatter_heads", _mut_scatter_heads_swapped),
+    ("scatter_qkv_head_chunk", _mut_scatter_qkv_reversed_sources),
+    ("gather_output_head_chunk", _mut_gather_output_slot_order),
 ]
 
 
