@@ -136,3 +136,19 @@ def test_pages_shape_ordinary_and_exchanges_full_size():
         torch.cuda.synchronize()
         assert np.array_equal(to_host_bits(pay[..., :D]), want_y[:, :, :, off:off + cnt])
     assert np.array_equal(to_host_bits(outs), q)
+
+
+def test_rows_beyond_one_grid_dimension():
+    """More than 65535 x 128 sequence rows per segment: the copy's row blocks grow to
+    256 rows so the grid's y extent stays within 65535 (16-byte head rows keep the
+    arrays at about 0.5 GB)."""
+    P, B, S, H, D = 2, 1, 65535 * 128 + 1000, 2, 8
+    x = np.random.default_rng(5).integers(0, 1 << 16, size=(P, B, S, H, D), dtype=np.uint16)
+    tx = _dev(x)
+    y = torch.empty((P, B, P * S, H // P, D), dtype=torch.bfloat16, device="cuda")
+    qb.ulysses_scatter_heads(tx, y)
+    back = torch.empty_like(tx)
+    qb.ulysses_gather_heads(y, back)
+    torch.cuda.synchronize()
+    assert np.array_equal(_host(y), oracle.scatter_heads(x))
+    assert np.array_equal(_host(back), x)
