@@ -16,31 +16,30 @@ Readings where the pages are silent (listed with reasons in the design notes):
     inv = 127 / amax (448 / amax), 0 when amax == 0, and code =
     round-half-even(x * inv) in FP32 (INT8 saturating to [-128, 127]; E4M3
     nearest, ties to even, saturating at +-448).
-  * K mean = (sum of K over the sequence) / U in FP32, the sum taken in a fixed
-    order: rows of a source rank in chunks of 256, each chunk summed row by row,
-    chunks in order, ranks in order.
+  * K mean = (sum of K over the whole exchanged sequence) / U, taken exactly and
+    rounded once to FP32: the pages fix FP32 statistics but no summation order,
+    so the oracle uses the one result every order approximates.
   * Rows at or beyond U get code 0 and take no part in any amax; S_pad = S
     rounded up to a multiple of 64, padded with code 0.
   * Group g of Q covers global rows [32 g, 32 g + 32); of K, [64 g, 64 g + 64).
 """
 from __future__ import annotations
 
+from fractions import Fraction
 from typing import Dict, List
 
 import numpy as np
 
 from .qnre_oracle import all_to_all, bf16_to_f64
 
-SUM_CHUNK = 256
 Q_GROUP = 32
 K_GROUP = 64
 V_PAD = 64
 INT8_DIV = np.float32(127.0)
 E4M3_MAX = np.float32(448.0)
 
-__all__ = ["decode16", "e4m3_decode", "e4m3_encode", "int8_quantize", "reciprocal", "sage2_k_sum",
-           "sage2_scatter_qkv",
-           "SUM_CHUNK", "Q_GROUP", "K_GROUP", "V_PAD"]
+__all__ = ["decode16", "e4m3_decode", "e4m3_encode", "int8_quantize", "reciprocal", "round_to_f32",
+           "sage2_k_mean", "sage2_scatter_qkv", "Q_GROUP", "K_GROUP", "V_PAD"]
 
 
 # ---------------------------------------------------------------------------
@@ -106,31 +105,68 @@ def decode16(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:
     raise ValueError(f"unsupported input dtype {dtype!r}")
 
 
-def sage2_k_sum(k_ranks: List[np.ndarray], dtype: str = "bf16") -> np.ndarray:
-    """FP32 sum of K over the global sequence, in the fixed order of the reading:
-    k_ranks[r] is rank r's [B, L, H, D]; returns [B, H, D] float32."""
-    total = None
-    for kr in k_ranks:
-        kf = decode16(kr, dtype)
-        L = kf.shape[1]
-        rank_sum = np.zeros((kf.shape[0], kf.shape[2], kf.shape[3]), np.float32)
-        for c0 in range(0, L, SUM_CHUNK):
-            acc = np.zeros_like(rank_sum)
-            for s in range(c0, min(L, c0 + SUM_CHUNK)):
-                acc = (acc + kf[:, s]).astype(np.float32)
-            rank_sum = (rank_sum + acc).astype(np.float32)
-        total = rank_sum if total is None else (total + rank_sum).astype(np.float32)
-    return total
+def round_to_f32(q: Fraction) -> np.float32:
+    """The float32 nearest to the rational q (ties to the even significand): the best
+    of the float32 neighbours of q's float64 approximation, compared exactly."""
+    c = np.float32(float(q))
+    best = None
+    for cand in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        key = (abs(Fraction(float(cand)) - q), int(np.float32(cand).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, np.float32(cand))
+    return best[1]
+
+
+def _exact_row_sums(x: np.ndarray, significant_bits: int) -> np.ndarray:
+    """Exact sum over axis 1 of x [B, S, H, D] (float64 decodes of 16-bit floats with
+    `significant_bits` bits each), as an object array of Fractions [B, H, D].
+
+    Where every partial sum of a column is a multiple of its smallest bit weight
+    below 2^53 of them, float64 addition in any order is exact; other columns are
+    summed as Fractions."""
+    n = x.shape[1]
+    nz = x != 0
+    _, e = np.frexp(x)                                   # |x| < 2^e, lowest bit 2^(e - significant_bits)
+    e_top = np.where(nz, e, -(1 << 20)).max(axis=1)
+    e_low = np.where(nz, e - significant_bits, 1 << 20).min(axis=1)
+    fits = ~nz.any(axis=1) | (np.log2(max(n, 1)) + 1 + e_top - e_low <= 53)
+    approx = x.sum(axis=1)
+    out = np.empty(approx.shape, dtype=object)
+    for idx in np.ndindex(approx.shape):
+        if fits[idx]:
+            out[idx] = Fraction(float(approx[idx]))
+        else:
+            b, h, d = idx
+            out[idx] = sum((Fraction(float(v)) for v in x[b, :, h, d]), Fraction(0))
+    return out
+
+
+def sage2_k_mean(k_ranks: List[np.ndarray], used_sequence: int, dtype: str = "bf16") -> np.ndarray:
+    """K mean per (batch, head, channel) over the global sequence: the exact sum of
+    every rank's K rows divided by the used length U, rounded once to FP32.
+    k_ranks[r] is rank r's [B, L, H, D]; returns [B, H, D] float32.  Rows at or past
+    U are zero on input ("Prepared Low-Precision QKV Exchange": zero-padded tail), so
+    summing every row sums the used prefix."""
+    k = np.concatenate([decode16(kr, dtype).astype(np.float64) for kr in k_ranks], axis=1)   # [B, S, H, D]
+    total = _exact_row_sums(k, 8 if dtype == "bf16" else 11)
+    U = int(used_sequence)
+    out = np.empty(total.shape, np.float32)
+    for idx in np.ndindex(total.shape):
+        out[idx] = round_to_f32(total[idx] / U)
+    return out
 
 
 def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ranks: List[np.ndarray],
-                      used_sequence: int, dtype: str = "bf16") -> List[Dict[str, np.ndarray]]:
+                      used_sequence: int, dtype: str = "bf16",
+                      with_k_scaled: bool = False) -> List[Dict[str, np.ndarray]]:
     """Sage2 encoding after the head exchange, for every virtual rank.
 
     q/k/v_ranks[r]: bf16 (or fp16) bits [B, L, H, D] of source rank r.  Returns, for each
     destination rank r2 (heads [r2*H/P, (r2+1)*H/P)), a dict with
     q, k: int8 [B, S, H/P, D]; v: E4M3 codes [B, D, H/P, S_pad];
     q_scale [B, H/P, ceil(U/32)], k_scale [B, H/P, ceil(U/64)], v_scale [B, H/P, D] (float32).
+    with_k_scaled adds "k_scaled": the fp32 values (K - mean) * 127 / amax that the K
+    codes round, [B, S, H/P, D] (0 past U).
     """
     P = len(q_ranks)
     B, L, H, D = q_ranks[0].shape
@@ -150,8 +186,7 @@ def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ra
         return [np.concatenate(rows, axis=1) for rows in all_to_all(sent)]   # [B, S, H_l, D] each
 
     qg, kg, vg = exchange(q_ranks), exchange(k_ranks), exchange(v_ranks)
-    k_total = sage2_k_sum(k_ranks, dtype)                # [B, H, D]
-    k_mean_all = (k_total / np.float32(U)).astype(np.float32)
+    k_mean_all = sage2_k_mean(k_ranks, U, dtype)         # [B, H, D]
     out = []
     live = np.arange(S) < U
     for r2 in range(P):
@@ -164,6 +199,7 @@ def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ra
         k_scale = np.zeros((B, H_l, wk), np.float32)
         q8 = np.zeros((B, S, H_l, D), np.int8)
         k8 = np.zeros((B, S, H_l, D), np.int8)
+        k_scaled = np.zeros((B, S, H_l, D), np.float32)
         for g in range(wq):
             rows = slice(g * Q_GROUP, min(U, (g + 1) * Q_GROUP))
             amax = np.abs(qf[:, rows]).max(axis=(1, 3))                       # [B, H_l]
@@ -173,12 +209,17 @@ def sage2_scatter_qkv(q_ranks: List[np.ndarray], k_ranks: List[np.ndarray], v_ra
             rows = slice(g * K_GROUP, min(U, (g + 1) * K_GROUP))
             amax = np.abs(ks[:, rows]).max(axis=(1, 3))
             k_scale[:, :, g] = (amax / INT8_DIV).astype(np.float32)
-            k8[:, rows] = int8_quantize(ks[:, rows], reciprocal(amax, INT8_DIV)[:, None, :, None])
+            inv = reciprocal(amax, INT8_DIV)[:, None, :, None]
+            k8[:, rows] = int8_quantize(ks[:, rows], inv)
+            k_scaled[:, rows] = (ks[:, rows] * inv).astype(np.float32)
         vamax = np.where(live[None, :, None, None], np.abs(vf), 0).max(axis=1)   # [B, H_l, D]
         v_scale = (vamax / E4M3_MAX).astype(np.float32)
         vq = (vf * reciprocal(vamax, E4M3_MAX)[:, None]).astype(np.float32)
         v8 = np.where(live[None, :, None, None], e4m3_encode(vq), 0).astype(np.uint8)  # [B, S, H_l, D]
         v_out = np.zeros((B, D, H_l, S_pad), np.uint8)
         v_out[..., :S] = v8.transpose(0, 3, 2, 1)
-        out.append({"q": q8, "k": k8, "v": v_out, "q_scale": q_scale, "k_scale": k_scale, "v_scale": v_scale})
+        res = {"q": q8, "k": k8, "v": v_out, "q_scale": q_scale, "k_scale": k_scale, "v_scale": v_scale}
+        if with_k_scaled:
+            res["k_scaled"] = k_scaled
+        out.append(res)
     return out

@@ -49,16 +49,18 @@ def dest_index(tokens, P, B, S, H):
 
 
 def sample_tokens(T, S, n=512, seed=0):
-    """Stratified token sample: every segment start/end, tile edges (multiples of 128 +-1), random rest."""
+    """Stratified token sample of a [P, B, S]-ordered problem of T tokens: always the
+    first and last token of every (rank, batch) segment of S tokens and of every
+    256-row pair tile and 128-row CTA half, then random tokens until there are at
+    least n.  The mandatory picks are never dropped, so the sample may exceed n."""
     rng = np.random.default_rng(seed)
-    picks = {0, T - 1}
+    picks = set()
     for t0 in range(0, T, S):
         picks.update({t0, min(T - 1, t0 + S - 1)})
-        if len(picks) > n // 2:
-            break
-    for t0 in range(0, T, 128 * max(1, T // (128 * 64))):
-        picks.update({t0, max(0, t0 - 1), min(T - 1, t0 + 127)})
+    for t0 in range(0, T, 128):
+        picks.update({t0, min(T - 1, t0 + 127)})
     rest = n - len(picks)
     if rest > 0:
-        picks.update(rng.choice(T, size=min(rest, T), replace=False).tolist())
-    return np.array(sorted(picks))[:max(n, 1)]
+        pool = np.setdiff1d(np.arange(T), np.fromiter(picks, dtype=np.int64))
+        picks.update(rng.choice(pool, size=min(rest, len(pool)), replace=False).tolist())
+    return np.array(sorted(picks))

@@ -210,7 +210,8 @@ def test_full_size_sampled_values(name):
     assert status == 0
     for t in out.values():  # every element rewritten (poisoned with NaN before)
         assert not bool(torch.isnan(t).any())
-    tok = sample_tokens(wl.T, wl.S, n=384)
+    tok = sample_tokens(wl.T, wl.S, n=640)
+    assert len(tok) >= 512
     x2 = inp.x.reshape(wl.T, wl.hidden)
     O = oracle.project_norm_rope(x2[tok], inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin,
                                  inp.positions.reshape(-1)[tok], wl.num_heads, wl.rope_style)

@@ -1,8 +1,9 @@
 """Pins for the Sage2 oracle: the E4M3 and INT8 encoders against the formats' definitions,
-the fixed-order K statistics against exact sums, and the encoding against invariants that
+the K mean against exact rational arithmetic, and the encoding against invariants that
 any correct grouped quantiser satisfies.  Planted mistakes must trip a pin."""
 import json
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -77,17 +78,71 @@ def check_int8_quantize():
     assert S2.reciprocal(np.array([3.0], np.float32), np.float32(448)).dtype == np.float32
 
 
-def check_k_sum_exact_and_ordered():
+def _f32_of_rational(q):
+    """Nearest float32 to the rational q, ties to even, by integer arithmetic: scale q
+    so that its float32 significand is an integer, round half to even, scale back."""
+    q = Fraction(q)
+    if q == 0:
+        return np.float32(0.0)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1                                            # now 2^e <= a < 2^(e+1)
+    e = max(e, -126)                                      # subnormals share the smallest exponent
+    m = round(a / Fraction(2) ** (e - 23))                # Fraction.__round__ ties to even
+    v = float(Fraction(m) * Fraction(2) ** (e - 23))
+    return np.float32(-v if q < 0 else v)
+
+
+def check_k_mean_exact():
+    """The K mean is the exact sum over the whole sequence divided by U, rounded once
+    to fp32, in every case: small integers, random values against rational arithmetic,
+    a column whose float32 sums (row by row, or in 256-row chunks) round differently,
+    and a column too wide for float64 summation."""
     rng = np.random.default_rng(31)
     P, B, L, H, D = 2, 1, 300, 2, 4
-    ints = rng.integers(-50, 51, size=(P, B, L, H, D)).astype(np.float32)   # sums of small integers are exact
+    ints = rng.integers(-50, 51, size=(P, B, L, H, D)).astype(np.float32)
     ks = [_bf16(ints[r]) for r in range(P)]
-    assert np.array_equal(S2.sage2_k_sum(ks), ints.sum(axis=(0, 2)))
-    vals = (rng.standard_normal((P, B, L, H, D)) * 3).astype(np.float32)
+    U = P * L
+    want = np.vectorize(lambda v: _f32_of_rational(Fraction(int(v), U)))(ints.sum(axis=(0, 2)))
+    assert np.array_equal(S2.sage2_k_mean(ks, U), want.astype(np.float32))
+    # random bf16 values, U shorter than the sequence (rows past U zero)
+    vals = (rng.standard_normal((P, B, L, H, D)) * 3 + 2).astype(np.float32)
+    U = 517
+    vals.reshape(P * L, H, D)[U:] = 0                    # B = 1: global row r*L + s, zero past U
     ks = [_bf16(vals[r]) for r in range(P)]
-    exact = np.stack([_f(k) for k in ks]).sum(axis=(0, 2))
-    got = S2.sage2_k_sum(ks).astype(np.float64)
-    assert np.abs(got - exact).max() < 1e-4 * np.abs(exact).max() + 1e-3
+    dec = np.stack([_f(k) for k in ks])                  # [P, B, L, H, D] exact values
+    got = S2.sage2_k_mean(ks, U)
+    for b, h, d in np.ndindex(B, H, D):
+        exact = sum((Fraction(float(v)) for v in dec[:, b, :, h, d].ravel()), Fraction(0)) / U
+        assert got[b, h, d] == _f32_of_rational(exact), (b, h, d)
+    # 2^24 followed by 299 ones: float32 sums lose the ones (row by row: 2^24; in
+    # 256-row chunks: 2^24 + 44); the exact mean keeps them
+    col = np.ones((1, 1, 300, 1, 1), np.float32)
+    col[0, 0, 0] = 2.0 ** 24
+    m = S2.sage2_k_mean([_bf16(col[0])], 300)
+    assert m[0, 0, 0] == _f32_of_rational(Fraction(2 ** 24 + 299, 300))
+    assert m[0, 0, 0] != np.float32(np.float32(2.0 ** 24) / np.float32(300))
+    assert m[0, 0, 0] != np.float32(np.float32(2.0 ** 24 + 44) / np.float32(300))
+    # 2^60 + 2^-60 - 2^60: float64 sums in row order give 0; the exact sum is 2^-60
+    wide = np.zeros((1, 1, 3, 1, 1), np.float32)
+    wide[0, 0, :, 0, 0] = [2.0 ** 60, 2.0 ** -60, -(2.0 ** 60)]
+    m = S2.sage2_k_mean([_bf16(wide[0])], 3)
+    assert m[0, 0, 0] == _f32_of_rational(Fraction(1, 3 * 2 ** 60)) and m[0, 0, 0] > 0
+
+
+def check_round_to_f32():
+    """round_to_f32 against the integer-arithmetic rounding above, at ties and between."""
+    rng = np.random.default_rng(34)
+    one = Fraction(1)
+    cases = [one / 3, -one / 3, Fraction(2 ** 24 + 1), Fraction(2 ** 24 + 3), Fraction(1, 2 ** 149),
+             Fraction(3, 2 ** 150), Fraction(10 ** 30, 7)]
+    cases += [Fraction(int(n), int(dn)) for n, dn in zip(rng.integers(-10 ** 12, 10 ** 12, 300),
+                                                        rng.integers(1, 10 ** 9, 300))]
+    for q in cases:
+        assert S2.round_to_f32(q) == _f32_of_rational(q), q
+    assert S2.round_to_f32(Fraction(2 ** 24 + 1)) == np.float32(2 ** 24)       # tie to the even significand
+    assert S2.round_to_f32(Fraction(2 ** 24 + 3)) == np.float32(2 ** 24 + 4)
 
 
 def _inputs(P=2, B=2, L=70, H=4, D=8, seed=32, smooth=None):
@@ -110,7 +165,7 @@ def check_sage2_structure_and_bounds():
         ex_q = oracle.scatter_heads(np.stack(q))   # [P, B, S, H_l, D] bf16 bits, pinned elsewhere
         ex_k = oracle.scatter_heads(np.stack(k))
         ex_v = oracle.scatter_heads(np.stack(v))
-        kmean = (S2.sage2_k_sum(k) / np.float32(U)).astype(np.float32)
+        kmean = S2.sage2_k_mean(k, U)
         for r in range(P):
             o = res[r]
             assert o["q"].shape == (B, S, H_l, D) and o["k"].shape == (B, S, H_l, D)
@@ -158,8 +213,9 @@ def check_decode16():
     assert S2.decode16(np.array([0x3F80], np.uint16), "bf16").tolist() == [1.0]
 
 
-CHECKS = [check_decode16, check_e4m3_rounding, check_e4m3_matches_brute_force, check_int8_quantize, check_k_sum_exact_and_ordered,
-          check_sage2_structure_and_bounds, check_sage2_smoothing_removes_channel_offset]
+CHECKS = [check_decode16, check_e4m3_rounding, check_e4m3_matches_brute_force, check_int8_quantize,
+          check_k_mean_exact, check_round_to_f32, check_sage2_structure_and_bounds,
+          check_sage2_smoothing_removes_channel_offset]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__)
@@ -186,8 +242,37 @@ def _mut_e4m3_ties_away(x):
     return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
 
 
-def _mut_k_sum_no_chunks(k_ranks, dtype="bf16"):
-    return np.stack([_f(k).astype(np.float32) for k in k_ranks]).sum(axis=(0, 2)).astype(np.float32) * np.float32(1.001)
+def _mut_k_mean_f32_rows(k_ranks, used_sequence, dtype="bf16"):
+    """float32 sum row by row, then / U: a plausible kernel order, not the definition."""
+    k = np.concatenate([S2.decode16(kr, dtype) for kr in k_ranks], axis=1)
+    acc = np.zeros((k.shape[0], k.shape[2], k.shape[3]), np.float32)
+    for s in range(k.shape[1]):
+        acc = (acc + k[:, s]).astype(np.float32)
+    return (acc / np.float32(used_sequence)).astype(np.float32)
+
+
+def _mut_k_mean_f32_chunks(k_ranks, used_sequence, dtype="bf16"):
+    """float32 sums of 256-row chunks, chunks in order, then / U."""
+    k = np.concatenate([S2.decode16(kr, dtype) for kr in k_ranks], axis=1)
+    total = np.zeros((k.shape[0], k.shape[2], k.shape[3]), np.float32)
+    for c0 in range(0, k.shape[1], 256):
+        acc = np.zeros_like(total)
+        for s in range(c0, min(k.shape[1], c0 + 256)):
+            acc = (acc + k[:, s]).astype(np.float32)
+        total = (total + acc).astype(np.float32)
+    return (total / np.float32(used_sequence)).astype(np.float32)
+
+
+def _mut_k_mean_over_all_rows(k_ranks, used_sequence, dtype="bf16"):
+    """divides by the whole sequence length instead of the used length U"""
+    n = sum(kr.shape[1] for kr in k_ranks)
+    return S2.__dict__["_orig_k_mean"](k_ranks, n, dtype)
+
+
+def _mut_round_to_f32_truncate(q):
+    """rounds toward zero instead of to nearest"""
+    c = np.float32(float(q))
+    return c if abs(Fraction(float(c))) <= abs(Fraction(q)) else np.nextafter(c, np.float32(0))
 
 
 def _mut_reciprocal_unguarded(amax, top):
@@ -203,9 +288,13 @@ def _mut_reciprocal_swapped(amax, top):
 @pytest.mark.parametrize("name,mutant", [("int8_quantize", _mut_int8_floor), ("e4m3_encode", _mut_e4m3_ties_away),
                                          ("reciprocal", _mut_reciprocal_unguarded),
                                          ("reciprocal", _mut_reciprocal_swapped),
-                                         ("sage2_k_sum", _mut_k_sum_no_chunks),
+                                         ("sage2_k_mean", _mut_k_mean_f32_rows),
+                                         ("sage2_k_mean", _mut_k_mean_f32_chunks),
+                                         ("sage2_k_mean", _mut_k_mean_over_all_rows),
+                                         ("round_to_f32", _mut_round_to_f32_truncate),
                                          ("Q_GROUP", 16), ("K_GROUP", 32), ("V_PAD", 128)])
 def test_sage2_pins_catch_planted_mistake(name, mutant, monkeypatch, golden_dir):
+    monkeypatch.setitem(S2.__dict__, "_orig_k_mean", S2.sage2_k_mean)
     monkeypatch.setattr(S2, name, mutant)
     tripped = []
     for check in CHECKS:

@@ -1,4 +1,5 @@
-"""The allocation-free forward (qnre_forward_noalloc) against the plan-based qnre_forward.
+"""The allocation-free forward (qnre_forward_noalloc) against the plan-based qnre_forward
+and the CPU oracle.
 
 qnre_forward_noalloc serves callers that cannot call cudaMalloc when they run
 the projection (a memory pool that forbids raw allocations, a runtime that owns
@@ -12,8 +13,9 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from ulysses_qkv_proj_gb300 import workloads as WL
-from _util import assert_fused_close, to_dev_bf16, to_host_f64
+from _util import assert_fused_close, to_dev_bf16, to_host_bits, to_host_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -31,13 +33,18 @@ def _noalloc():
     return fn
 
 
-def _inputs(wl, bad_positions=()):
+def _host_inputs(wl, bad_positions=()):
     inp = WL.make_fused_inputs(wl)
     if bad_positions:
         inp.positions = inp.positions.copy()
         flat = inp.positions.reshape(-1)
         for t in bad_positions:
             flat[t] = wl.n_pos + 5
+    return inp
+
+
+def _inputs(wl, bad_positions=(), inp=None):
+    inp = inp or _host_inputs(wl, bad_positions)
     return dict(x=to_dev_bf16(inp.x), w=to_dev_bf16(inp.w), qw=to_dev_bf16(inp.q_norm_w),
                 kw=to_dev_bf16(inp.k_norm_w), cs=torch.from_numpy(inp.cos_sin).cuda(),
                 pos=torch.from_numpy(inp.positions).cuda())
@@ -52,6 +59,9 @@ def _call_noalloc(fn, wl, d, out, status):
 
 
 def test_noalloc_forward_matches_plan_forward_on_two_calls_in_a_row():
+    """Two calls in a row.  Each output equals, bit for bit, a plan forward that takes
+    the same one-pair-per-cluster form (QNRE_FLAG_ONE_PAIR), and the CPU oracle
+    element by element within max(2 bf16 ulp, 2e-2)."""
     fn = _noalloc()
     calls = [
         # first call: one token with a position outside the table -> its q/k rows are NaN
@@ -63,9 +73,10 @@ def test_noalloc_forward_matches_plan_forward_on_two_calls_in_a_row():
     status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
     results = []
     for i, (wl, bad) in enumerate(calls):
-        d = _inputs(wl, bad)
+        inp = _host_inputs(wl, bad)
+        d = _inputs(wl, inp=inp)
         plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S,
-                       rope_style=wl.rope_style)
+                       rope_style=wl.rope_style, flags=qb.FLAG_ONE_PAIR)
         ref = qb.alloc_outputs(plan, wl.B, wl.S)
         qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], ref)
         out = qb.alloc_outputs(plan, wl.B, wl.S)
@@ -75,13 +86,16 @@ def test_noalloc_forward_matches_plan_forward_on_two_calls_in_a_row():
         assert st == 0, qb.STATUS_NAMES.get(st, st)
         torch.cuda.synchronize()
         plan_bits = plan.device_status()
-        results.append((wl, ref, out, plan_bits))
+        results.append((wl, inp, ref, out, plan_bits))
     bits = status.cpu().tolist()
-    assert bits[0] == qb.DEVICE_BAD_POSITION and results[0][3] == qb.DEVICE_BAD_POSITION
-    assert bits[1] == 0 and results[1][3] == 0
-    for wl, ref, out, _ in results:
+    assert bits[0] == qb.DEVICE_BAD_POSITION and results[0][4] == qb.DEVICE_BAD_POSITION
+    assert bits[1] == 0 and results[1][4] == 0
+    for wl, inp, ref, out, _ in results:
+        want = oracle.qnre_forward(inp.x, inp.w, inp.q_norm_w, inp.k_norm_w, inp.cos_sin, inp.positions,
+                                   wl.P, wl.num_heads, wl.layout, wl.rope_style)
         for g in ref:
-            assert_fused_close(to_host_f64(out[g]), to_host_f64(ref[g]), what=f"{wl.name}/{g}")
+            assert np.array_equal(to_host_bits(out[g]), to_host_bits(ref[g])), f"{wl.name}/{g}"
+            assert_fused_close(to_host_f64(out[g]), want[g], what=f"{wl.name}/{g}")
 
 
 def test_noalloc_rejects_before_enqueueing():

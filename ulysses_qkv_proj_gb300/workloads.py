@@ -121,9 +121,13 @@ HEADCHUNK_WORKLOADS: Dict[str, HeadChunkWorkload] = {
         schedule=((0, 7), (7, 14), (21, 7))),
 }
 
-# The benchmarked step runs the fused op on this shape, and the head-chunk pack
-# and merge over the same Q/K/V geometry with an uneven schedule over H_local = 8.
-BENCH_FUSED = "h4096_p4_s4096"
+# The benchmarked step runs the fused op on the largest fused shape, and the
+# head-chunk pack and merge over the same Q/K/V geometry with an uneven schedule
+# over H_local = 8.  Beside it the benchmark times the fused op alone on the
+# 4096-token shape and the pack/merge alone on the pages' head-chunk shape.
+BENCH_FUSED = "h8192_p8_b2_s16384"
+BENCH_FUSED_SMALL = "h4096_p4_s4096"
+BENCH_HEADCHUNK = "headchunk_p2_s37760_h56"
 BENCH_SCHEDULE: Tuple[Tuple[int, int], ...] = ((0, 2), (2, 4), (6, 2))
 
 
