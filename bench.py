@@ -235,6 +235,13 @@ class ClockSampler:
                 "region_s": round(t1 - t0, 4)}
 
 
+def pci_bus_id(torch, dev) -> str:
+    """PCI bus id of the CUDA device as NVML and nvidia-smi name it (domain:bus:device.0)."""
+    props = torch.cuda.get_device_properties(dev)
+    return "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
+                                 getattr(props, "pci_device_id", 0))
+
+
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
@@ -245,6 +252,8 @@ class Gpu:
         self.torch = torch
         self.dev = dev
         self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+        khz = getattr(torch.cuda.get_device_properties(dev), "clock_rate", 0) or 2_000_000
+        self.sleep_cycles = int(2e-3 * khz * 1e3)  # about 2 ms of GPU time
 
     def bf16(self, a):
         t = self.torch
@@ -252,7 +261,10 @@ class Gpu:
 
     def timed_alone(self, fn, steps: int, warmup: int):
         """Mean and median CUDA-event time (ms) of fn() on the current stream, L2
-        flushed between repetitions (outside the events)."""
+        flushed between repetitions (outside the events).  Each repetition is queued
+        behind a 2 ms GPU sleep, so fn's launches run back to back on the device
+        however long the host takes to enqueue them: the events time the kernels,
+        not the Python calls between them."""
         torch = self.torch
         for _ in range(warmup):
             fn()
@@ -260,6 +272,7 @@ class Gpu:
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in evs:
+            torch.cuda._sleep(self.sleep_cycles)
             a.record()
             fn()
             b.record()
@@ -294,7 +307,7 @@ def time_fused_alone(gpu, qb, wl, peaks, peak_src, steps, warmup):
             "tflops": round(tflops, 1), "tokens_per_s": round(wl.T / (ms * 1e-3), 1),
             "frac": round(tflops / peak, 4), "peak": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
             "clusters": info["clusters"], "pairs_per_cluster": info["pairs_per_cluster"],
-            "launches": steps, "timing": "alone, L2 flushed between launches"}
+            "launches": steps, "timing": "alone, launch queued behind a GPU sleep, L2 flushed between launches"}
 
 
 def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra=True):
@@ -310,23 +323,30 @@ def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra
               for _ in range(P)]
     merged = [torch.empty((wl.B, S, wl.num_heads, D), dtype=torch.bfloat16, device=gpu.dev) for _ in range(P)]
     offs = [off for off, _ in wl.schedule]
+    n_chunks = len(wl.schedule)
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
 
     def row(ms, med, nbytes, launches, form):
         g = nbytes / (ms * 1e-3) / 1e9
         return {"ms": round(ms, 5), "ms_median": round(med, 5), "bytes": nbytes, "GB/s": round(g, 1),
                 "frac_hbm": round(g / hbm, 4), "peak": hbm, "peak_source": f"{peak_src} hbm_gbs",
-                "launches": launches, "form": form}
+                "launches": launches, "form": form,
+                "timing": "alone, launches queued behind a GPU sleep, L2 flushed between repetitions"}
 
     def pack_chunks():
         for r, (q, k, v) in enumerate(views):
             for i, (off, cnt) in enumerate(wl.schedule):
                 qb.ulysses_pack_head_chunk(q, k, v, W, off, cnt, packed[r][i])
 
+    # the merge input of each chunk: the gathered output band, contiguous
+    # [B, S, W*cnt, D] as the pages define it (here the packed q slice, so pack then
+    # merge reproduces q)
+    received = [[None] * n_chunks for _ in range(P)]
+
     def merge_chunks():
         for r in range(P):
             for i, off in enumerate(offs):
-                qb.ulysses_merge_output_head_chunk(packed[r][i][..., :D], W, L, off, merged[r])
+                qb.ulysses_merge_output_head_chunk(received[r][i], W, L, off, merged[r])
 
     def pack_sched():
         for r, (q, k, v) in enumerate(views):
@@ -334,13 +354,15 @@ def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra
 
     def merge_sched():
         for r in range(P):
-            qb.ulysses_merge_output_head_chunk_schedule([pk[..., :D] for pk in packed[r]], W, L, offs, merged[r])
+            qb.ulysses_merge_output_head_chunk_schedule(received[r], W, L, offs, merged[r])
 
     pack_bytes = sum(2 * wl.B * S * W * cnt * 3 * D * 2 for _, cnt in wl.schedule) * P
     merge_bytes = sum(2 * wl.B * S * W * cnt * D * 2 for _, cnt in wl.schedule) * P
-    n_chunks = len(wl.schedule)
     res = {}
     ms, med = gpu.timed_alone(pack_chunks, steps, warmup)
+    for r in range(P):
+        for i in range(n_chunks):
+            received[r][i] = packed[r][i][..., :D].contiguous()
     res["pack_per_chunk"] = row(ms, med, pack_bytes, P * n_chunks, "ulysses_pack_head_chunk, one launch per chunk "
                                                                    "and virtual rank")
     ms, med = gpu.timed_alone(merge_chunks, steps, warmup)
@@ -416,10 +438,7 @@ def run_gpu(args):
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    props = torch.cuda.get_device_properties(dev)
-    pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
-                                getattr(props, "pci_device_id", 0))
-    clocks = ClockSampler(pci).start()
+    clocks = ClockSampler(pci_bus_id(torch, dev)).start()
     gpu = Gpu(torch, dev)
     wl = WORKLOAD
     peaks, peak_src = load_peaks()
@@ -761,11 +780,13 @@ def run_gpu_workload(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     gpu = Gpu(torch, dev)
+    clocks = ClockSampler(pci_bus_id(torch, dev)).start()
     peaks, peak_src = load_peaks()
     name = args.workload
     if name in WL.FUSED_WORKLOADS:
         wl = WL.FUSED_WORKLOADS[name]
-        res = time_fused_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup)
+        with clocks.section("alone"):
+            res = time_fused_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup)
         line = {"metric": "fused QKV+norm+RoPE+scatter tokens/s", "value": res["tokens_per_s"], "unit": "tokens/s",
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
                 "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
@@ -798,7 +819,8 @@ def run_gpu_workload(args):
             plan.destroy()
     elif name in WL.HEADCHUNK_WORKLOADS:
         wl = WL.HEADCHUNK_WORKLOADS[name]
-        res = time_headchunk_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup, rows_extra=True)
+        with clocks.section("alone"):
+            res = time_headchunk_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup, rows_extra=True)
         p = res["pack_per_chunk"]
         line = {"metric": "head-chunk pack/merge GB/s", "value": p["GB/s"], "unit": "GB/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": p["ms"], "higher_is_better": True,
@@ -810,6 +832,8 @@ def run_gpu_workload(args):
         line.update(res)
     else:
         raise SystemExit(f"unknown workload {name!r}")
+    clocks.stop()
+    line["clocks"] = clocks.summary("alone")
     print(json.dumps(line), flush=True)
 
 

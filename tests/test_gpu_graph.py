@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from ulysses_qkv_proj_gb300 import workloads as WL
+from _sage2 import assert_sage2_matches, sage2_oracle
 from _util import assert_fused_close, to_dev_bf16, to_host_bits, to_host_f64
 
 torch = pytest.importorskip("torch")
@@ -97,9 +98,4 @@ def test_sage2_replay_with_fresh_inputs():
         graph.replay()
         torch.cuda.synchronize()
         ranks = bits.reshape(P, B, L, 3, H, D)
-        ref = oracle.sage2_scatter_qkv([ranks[r][:, :, 0] for r in range(P)], [ranks[r][:, :, 1] for r in range(P)],
-                                       [ranks[r][:, :, 2] for r in range(P)], U)
-        for r in range(P):
-            for key in ("q", "k", "v", "q_scale", "k_scale", "v_scale"):
-                got = enc[key][r].cpu().numpy()
-                assert got.tobytes() == np.ascontiguousarray(ref[r][key]).tobytes(), f"replay {replay} rank {r} {key}"
+        assert_sage2_matches(enc, sage2_oracle(ranks, U, "bf16"), P)

@@ -88,6 +88,16 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
   }
 }
 
+#ifndef QNRE_X_POLICY
+#define QNRE_X_POLICY 0  // L2 priority of the x loads: 0 evict_last, 1 evict_normal, 2 evict_first
+#endif
+#ifndef QNRE_W_POLICY
+#define QNRE_W_POLICY 0  // the same for the W loads
+#endif
+__device__ __forceinline__ uint64_t l2_policy(int kind) {
+  return kind == 0 ? ptx::l2_policy_evict_last() : (kind == 1 ? ptx::l2_policy_evict_normal() : ptx::l2_policy_evict_first());
+}
+
 __device__ __forceinline__ void grace_spin(uint64_t ns) {
   const uint64_t t0 = ptx::global_timer_ns();
   while (ptx::global_timer_ns() - t0 < ns) {
@@ -170,8 +180,8 @@ template <int kPC>
 __device__ void run_producer(const FusedArgs& a, const SmemLayout& L, volatile uint32_t* abort_flag) {
   uint32_t g = 0;
   uint32_t used_mask = 0, parity_mask = 0;  // per stage: ever loaded / parity of its last load
-  const uint64_t pol_x = ptx::l2_policy_evict_last();
-  const uint64_t pol_w = ptx::l2_policy_evict_last();
+  const uint64_t pol_x = l2_policy(QNRE_X_POLICY);
+  const uint64_t pol_w = l2_policy(QNRE_W_POLICY);
   const uint32_t full_leader = ptx::mapa_shared(L.full, L.leader);
   const uint32_t q = L.crank >> 1;  // pair in the cluster
   const int unit = blockIdx.x / (2 * kPC);
