@@ -29,9 +29,13 @@
 //   * warps 2-5 of each CTA: epilogue; thread i owns TMEM lane i = token row i
 //     of that CTA's half, so a head's 128 values are thread-local: the RMS sum,
 //     the scale and both RoPE pairings need no cross-thread traffic; the bf16
-//     rows go through a swizzled 8 KiB per-warp staging buffer so each store
-//     instruction writes two whole 256-byte head rows of the band destination;
-//     then both CTAs release the accumulator on the leader.
+//     rows go into an 8 KiB per-warp staging buffer (two 32 x 128-byte halves,
+//     128-byte swizzle), and when the warp's 32 tokens lie in one (rank, batch)
+//     segment one lane writes them into the head's band with two TMA tensor
+//     stores (box 64 columns x 32 consecutive band rows); otherwise (a segment
+//     edge, the ragged end, the publishing form, the debug build) each store
+//     instruction writes two whole 256-byte head rows; then both CTAs release
+//     the accumulator on the leader.
 //   * every mbarrier wait has a time limit; on expiry the kernel raises a
 //     status bit, tells the peer CTA to stop, drains its own in-flight copies
 //     and MMAs, frees its tensor memory and returns.
@@ -306,8 +310,13 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
   const int S_g = a.P * a.S;
   const int three_h = 3 * a.H;
   const uint32_t tempty_leader = ptx::mapa_shared(L.tempty, L.leader);
-  uint4* stage = epi_stage + (warp - 2) * (32 * 16);  // 32 rows x 256 B for this warp
-  uint4* stage_row = stage + lane * 16;
+  // This warp's staging: two 32 x 128-byte halves (columns 0-63, 64-127) in the
+  // 128-byte swizzle layout: 16-byte chunk c of row i sits at chunk (c ^ (i & 7))
+  // of that row, so neither the row-wise writes below nor the reads of either
+  // store path collide in a bank, and a TMA store can read each half directly.
+  uint4* stage = epi_stage + (warp - 2) * (kEpiWarpBytes / 16);
+  const uint32_t stage_saddr = ptx::smem_addr(stage);
+  bool store_pending = false;  // lane 0: a TMA store may still be reading the staging
   const int unit = blockIdx.x / (2 * kPC);
   const int num_units = gridDim.x / (2 * kPC);
   uint32_t it = 0;
@@ -339,6 +348,12 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
       bad_pos = pos < 0 || pos >= a.n_pos;
     }
     const long long dest_row = static_cast<long long>(r_s) * a.S + s_loc;  // global row in batch b
+    // The warp's 32 tokens t - lane .. t - lane + 31 go to 32 consecutive rows of
+    // every head band when they are all valid and lie in one (rank, batch)
+    // segment: then one TMA store box covers them (lane 0's token is the first).
+    const int t_first = t - lane;
+    const bool tma_rows = !QNRE_DEBUG_BOUNDS && a.tma_store && a.ready == nullptr &&
+                          t_first + (kStoreRows - 1) < a.T && (t_first % a.S) + (kStoreRows - 1) < a.S;
 
 #pragma unroll 1
     for (int hh = 0; hh < tw.width / 128; ++hh) {
@@ -462,9 +477,15 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
             hi[i] = __uint_as_float(0x7FC00000u);
           }
         }
-        // Stage the bf16 row in this warp's buffer: row `lane`, 16-byte chunk
-        // c at chunk slot c ^ (lane & 15) so that neither these writes nor the
-        // row-wise reads below collide in the same banks.
+        // The previous head's TMA store must have read the staging before it
+        // is rewritten.
+        if (p == 0 && store_pending) {
+          ptx::bulk_wait_group_read_all();
+          store_pending = false;
+        }
+        __syncwarp();
+        // Stage the bf16 row in this warp's buffer: row `lane`, 16-byte chunk c
+        // (8 columns) in half c / 8 at swizzled chunk (c % 8) ^ (lane % 8).
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint4 u;
@@ -472,19 +493,37 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
           u.y = pack_bf16x2(lo[8 * j + 2], lo[8 * j + 3]);
           u.z = pack_bf16x2(lo[8 * j + 4], lo[8 * j + 5]);
           u.w = pack_bf16x2(lo[8 * j + 6], lo[8 * j + 7]);
-          stage_row[(c_lo / 8 + j) ^ (lane & 15)] = u;
+          const int cl = c_lo / 8 + j;
+          stage[(cl >> 3) * (kEpiHalfBytes / 16) + lane * 8 + ((cl & 7) ^ (lane & 7))] = u;
           uint4 w;
           w.x = pack_bf16x2(hi[8 * j + 0], hi[8 * j + 1]);
           w.y = pack_bf16x2(hi[8 * j + 2], hi[8 * j + 3]);
           w.z = pack_bf16x2(hi[8 * j + 4], hi[8 * j + 5]);
           w.w = pack_bf16x2(hi[8 * j + 6], hi[8 * j + 7]);
-          stage_row[(c_hi / 8 + j) ^ (lane & 15)] = w;
+          const int ch2 = c_hi / 8 + j;
+          stage[(ch2 >> 3) * (kEpiHalfBytes / 16) + lane * 8 + ((ch2 & 7) ^ (lane & 7))] = w;
         }
       }
-      // Write the warp's 32 head rows back two rows per instruction: lanes
-      // 0-15 cover row 2i and lanes 16-31 row 2i+1, 256 contiguous bytes each.
-      __syncwarp();
-      {
+      if (tma_rows) {
+        // Two TMA stores (columns 0-63 and 64-127) write the warp's 32 rows of
+        // this head into its band: box 64 x 1 x 32 at (column, local head,
+        // flattened (rank, batch, global row)).  The staging writes are made
+        // visible to the async proxy first.
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const CUtensorMap* map = &a.tmap_out[a.layout == 0 ? g : 0];
+          const int col = a.layout == 0 ? 0 : g * 128;
+          const int grow = static_cast<int>((static_cast<long long>(r) * a.B + b) * S_g + dest_row);
+          ptx::tma_store_3d(map, stage_saddr, col, hl, grow);
+          ptx::tma_store_3d(map, stage_saddr + kEpiHalfBytes, col + 64, hl, grow);
+          ptx::bulk_commit_group();
+          store_pending = true;
+        }
+      } else {
+        // Write the warp's 32 head rows back two rows per instruction: lanes
+        // 0-15 cover row 2i and lanes 16-31 row 2i+1, 256 contiguous bytes each.
+        __syncwarp();
         const int half = lane >> 4;
         const int chunk = lane & 15;
 #pragma unroll 4
@@ -492,7 +531,8 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
           const int src_row = 2 * i + half;
           uint4* rd = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<long long>(d4), src_row));
           const int rv = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, src_row);
-          const uint4 u = stage[src_row * 16 + (chunk ^ (src_row & 15))];
+          const uint4 u =
+              stage[(chunk >> 3) * (kEpiHalfBytes / 16) + src_row * 8 + ((chunk & 7) ^ (src_row & 7))];
           if (rv) rd[chunk] = u;
         }
       }
@@ -511,6 +551,9 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader + 8 * acc);
   }
+  // Every TMA store has completed before the CTA (and its shared memory) ends.
+  if (lane == 0 && store_pending) ptx::bulk_wait_group_all();
+  __syncwarp();
 }
 
 template <int kPC>
@@ -523,13 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   SmemLayout L;
   L.a = raw + pad;
   L.b = L.a + kStages * kABytes;
-  const uint32_t bar0 = L.b + kStages * kBBytes;
+  const uint32_t bar0 = L.b + kStages * kBBytes + kEpiStageBytes;
   L.full = bar0;
   L.empty = L.full + 8 * kStages;
   L.tfull = L.empty + 8 * kStages;
   L.tempty = L.tfull + 16;
   L.drain = L.tempty + 16;
-  uint8_t* bar_ptr = smem + kStages * kStageBytes;
+  uint4* epi_stage = reinterpret_cast<uint4*>(smem + kStages * kStageBytes);  // 1024-byte aligned
+  uint8_t* bar_ptr = smem + kStages * kStageBytes + kEpiStageBytes;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * kStages + 5));
   volatile uint32_t* abort_flag = tmem_holder + 1;
   L.abort = ptx::smem_addr(tmem_holder + 1);
@@ -538,7 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   L.leader = L.crank & ~1u;
   L.ncta = 2u * kPC;
   float* norm_w = reinterpret_cast<float*>(bar_ptr + kBarBytes);
-  uint4* epi_stage = reinterpret_cast<uint4*>(bar_ptr + kBarBytes + 2 * 128 * 4);  // 16-byte aligned
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -546,6 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_qkv_kernel(const __grid_con
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&args.tmap_x);
     ptx::prefetch_tensormap(&args.tmap_w);
+    if (args.tma_store) {
+      for (int i = 0; i < (args.layout == 0 ? 3 : 1); ++i) ptx::prefetch_tensormap(&args.tmap_out[i]);
+    }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(L.full + 8 * s, 1);   // the leader's expect_tx arrival
       ptx::mbar_init(L.empty + 8 * s, kPC);  // one multicast commit from each pair that reads the stage

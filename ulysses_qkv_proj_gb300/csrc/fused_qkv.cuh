@@ -33,7 +33,12 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAccCols = kBN;                 // fp32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator
 constexpr int kBarBytes = 256;                // mbarriers + small words
-constexpr int kEpiStageBytes = 4 * 32 * 256;  // one 32-row x 256 B bf16 head tile per epilogue warp
+// One 32-row bf16 head tile per epilogue warp, as two 32 x 128-byte halves
+// (columns 0-63 and 64-127) in the 128-byte swizzle layout that TMA stores read.
+constexpr int kEpiHalfBytes = 32 * 128;
+constexpr int kEpiWarpBytes = 2 * kEpiHalfBytes;
+constexpr int kEpiStageBytes = 4 * kEpiWarpBytes;
+constexpr int kStoreRows = 32;  // rows per TMA store box (one epilogue warp's tokens)
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
                            2 * 128 * 4 /*norm weights*/ + kEpiStageBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a limit");
@@ -41,6 +46,11 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a l
 struct FusedArgs {
   CUtensorMap tmap_x;  // bf16 [T, K], box 64 x 128, 128-byte swizzle
   CUtensorMap tmap_w;  // bf16 [K, N], box 64 x 64, 128-byte swizzle
+  // Head-band outputs for TMA stores (when tma_store): bshd q, k, v as
+  // [P*B*S_g, H_local, 128], or the fused payload (index 0) as
+  // [P*B*S_g, H_local, 384]; box 64 x 1 x 32, 128-byte swizzle.
+  CUtensorMap tmap_out[3];
+  int tma_store;  // 1: warps whose 32 tokens sit in one segment store their head rows with TMA
   const uint16_t* q_norm_w;
   const uint16_t* k_norm_w;
   const float* cos_sin;

@@ -86,6 +86,21 @@ bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Head-band output for TMA stores: bf16 [rows, H_local, width] (width 128 for a
+// bshd q/k/v tensor, 384 for the fused payload), box 64 x 1 x 32 with the
+// 128-byte swizzle the epilogue's staging uses.
+bool encode_out_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t H_local, uint64_t width) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {width, H_local, rows};
+  const cuuint64_t strides[2] = {width * 2, H_local * width * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(qnre::kStoreRows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -320,6 +335,20 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.out_fused = static_cast<uint16_t*>(bshd ? nullptr : out->fused);
   a.status = plan->d_status;
   a.ready = ready;
+  // TMA stores of whole 32-row head tiles (their row coordinate is 32-bit); the
+  // debug build and the publishing form store rows one by one.
+  {
+    const int64_t band_rows = T * P;  // P * B * S_global rows of each band tensor
+    bool ok = !QNRE_DEBUG_BOUNDS && ready == nullptr && band_rows < (int64_t{1} << 31);
+    if (ok && bshd) {
+      ok = encode_out_bf16(&a.tmap_out[0], out->q, band_rows, plan->H_local, 128) &&
+           encode_out_bf16(&a.tmap_out[1], out->k, band_rows, plan->H_local, 128) &&
+           encode_out_bf16(&a.tmap_out[2], out->v, band_rows, plan->H_local, 128);
+    } else if (ok) {
+      ok = encode_out_bf16(&a.tmap_out[0], out->fused, band_rows, plan->H_local, 384);
+    }
+    a.tma_store = ok ? 1 : 0;
+  }
   // [P, B, P*S_local, H_local, D] = T * H * D elements (T = P*B*S_local tokens)
   a.out_elems = static_cast<long long>(T) * plan->num_heads * (bshd ? 128 : 384);
 #if QNRE_DEBUG_BOUNDS
