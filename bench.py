@@ -537,16 +537,17 @@ def run_gpu(args):
     h2d = x_host.numel() * 2 + qkv_host.numel() * 2
     d2h = sum(t.numel() * 2 for t in out.values()) + merged.numel() * 2
     h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    n = args.steps
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_comp = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     main = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-    with clocks.section("e2e"):
-        e2e_start.record(main)
-        h2d_s.wait_event(e2e_start)
+
+    def e2e_pass(n):
+        """n pipelined steps with their host copies; returns the device time (ms) of all n."""
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_comp = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e_start.record(main)
+        h2d_s.wait_event(e_start)
         for i in range(n):
             b = i % 2
             xin, qin = dev_in[b]
@@ -569,9 +570,17 @@ def run_gpu(args):
                 hm.copy_(sets[b]["merged"], non_blocking=True)
             ev_out[i].record(d2h_s)
         main.wait_stream(d2h_s)
-        e2e_end.record(main)
+        e_end.record(main)
         torch.cuda.synchronize()
-    e2e_ms = e2e_start.elapsed_time(e2e_end) / n
+        return e_start.elapsed_time(e_end)
+
+    # the first copy from or into a freshly pinned buffer pays its mapping (tens
+    # of ms): warm-up passes touch every buffer before the timed one
+    e2e_pass(max(2, args.warmup))
+    n = args.steps
+    with clocks.section("e2e"):
+        e2e_total = e2e_pass(n)
+    e2e_ms = e2e_total / n
     if not torch.equal(host_out[1], qkv_host[:, :, 0]):
         raise RuntimeError("end-to-end result differs")
     if not torch.equal(host_out[0]["q"], out["q"].cpu()):
