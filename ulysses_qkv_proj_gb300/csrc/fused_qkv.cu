@@ -27,7 +27,8 @@
 //     double-buffering the accumulator so the epilogue of tile i overlaps the
 //     main loop of tile i+1; commits are multicast to both CTAs;
 //   * warps 2-5 of each CTA: epilogue; thread i owns TMEM lane i = token row i
-//     of that CTA's half, so a head's 128 values are thread-local: the RMS sum,
+//     of that CTA's half and reads a head's 128 accumulator columns once into
+//     registers, so they are thread-local: the RMS sum,
 //     the scale and both RoPE pairings need no cross-thread traffic; the bf16
 //     rows go into an 8 KiB per-warp staging buffer (two 32 x 128-byte halves,
 //     128-byte swizzle), and when the warp's 32 tokens lie in one (rank, batch)
@@ -388,22 +389,29 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
       const bool row_ok = valid;
 #endif
 
-      // Pass 1 (q, k): mean square of the head row.
+      // One read of the head's 128 accumulator columns: v[j] holds columns
+      // [32j, 32j + 32) of this thread's token.
+      uint32_t v[4][32];
+      ptx::tmem_ld_32x32b_x32(taddr, v[0]);
+      ptx::tmem_ld_32x32b_x32(taddr + 32, v[1]);
+      ptx::tmem_ld_32x32b_x32(taddr + 64, v[2]);
+      ptx::tmem_ld_32x32b_x32(taddr + 96, v[3]);
+      ptx::tmem_ld_wait();
+      reg_fence(v[0]);
+      reg_fence(v[1]);
+      reg_fence(v[2]);
+      reg_fence(v[3]);
+      // q, k: mean square of the head row (columns 0-31 with 32-63, then 64-95
+      // with 96-127, one pair of squares at a time).
       float scale = 1.0f;
       if (normed) {
         float ss = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t r0[32], r1[32];
-          ptx::tmem_ld_32x32b_x32(taddr + half * 64, r0);
-          ptx::tmem_ld_32x32b_x32(taddr + half * 64 + 32, r1);
-          ptx::tmem_ld_wait();
-          reg_fence(r0);
-          reg_fence(r1);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x0 = __uint_as_float(r0[i]);
-            const float x1 = __uint_as_float(r1[i]);
+            const float x0 = __uint_as_float(v[2 * half][i]);
+            const float x1 = __uint_as_float(v[2 * half + 1][i]);
             ss = fmaf(x0, x0, ss);
             ss = fmaf(x1, x1, ss);
           }
@@ -415,26 +423,20 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
       const bool nan_out = normed && bad_pos;
       const bool rope = normed && !bad_pos;
 
-      // Pass 2: scale, rotate, round, store.  Work on 64 columns at a time:
-      // rotate-half pairs column i with i + 64, so step p takes columns
-      // [32p, 32p + 32) and [64 + 32p, 96 + 32p); interleaved pairs are
-      // adjacent, so step p takes [64p, 64p + 64).
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const bool rh = a.rope_style == 0;
+      // Scale, rotate, round and stage 64 columns per step: rotate-half pairs
+      // column i with i + 64, so step p takes columns [32p, 32p + 32) and
+      // [64 + 32p, 96 + 32p) (v[p], v[2 + p]); interleaved pairs are adjacent, so
+      // step p takes [64p, 64p + 64) (v[2p], v[2p + 1]).  The call sites below
+      // fix which register blocks (vl, vh) a step pairs, so no register is
+      // selected at run time.
+      auto step = [&](const uint32_t(&vl)[32], const uint32_t(&vh)[32], const int p, const bool rh) {
         const int c_lo = rh ? 32 * p : 64 * p;
         const int c_hi = rh ? 64 + 32 * p : 64 * p + 32;
-        uint32_t r0[32], r1[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c_lo, r0);
-        ptx::tmem_ld_32x32b_x32(taddr + c_hi, r1);
-        ptx::tmem_ld_wait();
-        reg_fence(r0);
-        reg_fence(r1);
         float lo[32], hi[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          lo[i] = __uint_as_float(r0[i]);
-          hi[i] = __uint_as_float(r1[i]);
+          lo[i] = __uint_as_float(vl[i]);
+          hi[i] = __uint_as_float(vh[i]);
         }
         if (normed) {
 #pragma unroll
@@ -461,12 +463,12 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
             for (int i4 = 0; i4 < 8; ++i4) {
               const float4 c = __ldg(cs + 8 * p + i4);
               const float4 sn = __ldg(cs + 16 + 8 * p + i4);
-              float* v = i4 < 4 ? lo : hi;
+              float* pv = i4 < 4 ? lo : hi;
               const int o = (i4 & 3) * 8;
-              rotate(v[o + 0], v[o + 1], c.x, sn.x);
-              rotate(v[o + 2], v[o + 3], c.y, sn.y);
-              rotate(v[o + 4], v[o + 5], c.z, sn.z);
-              rotate(v[o + 6], v[o + 7], c.w, sn.w);
+              rotate(pv[o + 0], pv[o + 1], c.x, sn.x);
+              rotate(pv[o + 2], pv[o + 3], c.y, sn.y);
+              rotate(pv[o + 4], pv[o + 5], c.z, sn.z);
+              rotate(pv[o + 6], pv[o + 7], c.w, sn.w);
             }
           }
         }
@@ -503,6 +505,13 @@ __device__ void run_epilogue(const FusedArgs& a, const SmemLayout& L, uint32_t t
           const int ch2 = c_hi / 8 + j;
           stage[(ch2 >> 3) * (kEpiHalfBytes / 16) + lane * 8 + ((ch2 & 7) ^ (lane & 7))] = w;
         }
+      };
+      if (a.rope_style == 0) {
+        step(v[0], v[2], 0, true);
+        step(v[1], v[3], 1, true);
+      } else {
+        step(v[0], v[1], 0, false);
+        step(v[2], v[3], 1, false);
       }
       if (tma_rows) {
         // Two TMA stores (columns 0-63 and 64-127) write the warp's 32 rows of
