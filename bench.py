@@ -22,7 +22,10 @@ launches, L2 flushed between repetitions):
   * "pack" / "merge": the head-chunk pack and merge of [1, 37760, 56, 128] over
     two virtual ranks with the schedule [7, 14, 7] (the pages' shape), per
     chunk and as schedule calls;
-  * "fused_h4096_p4_s4096": the fused op alone on the 4096-token workload.
+  * "fused_h4096_p4_s4096": the fused op alone on the 4096-token workload;
+  * "fused_alone" and "unfused_torch": the headline workload's fused op alone,
+    and the same operator as separate PyTorch ops (cuBLAS GEMM, RMSNorm, RoPE,
+    band scatter) with the fused kernel's speedup over it.
 
 This benchmark runs on one GPU: it refuses WORLD_SIZE > 1 and --gpus > 1 (the
 fused kernel's two-pair clusters multicast W inside a cluster, and nothing on
@@ -291,9 +294,9 @@ def fused_setup(gpu, qb, wl, inp=None):
     return inp, d, plan
 
 
-def time_fused_alone(gpu, qb, wl, peaks, peak_src, steps, warmup):
+def time_fused_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, inp=None):
     """The fused op alone on `wl`; fraction of the burst tensor peak."""
-    _, d, plan = fused_setup(gpu, qb, wl)
+    _, d, plan = fused_setup(gpu, qb, wl, inp)
     out = qb.alloc_outputs(plan, wl.B, wl.S, gpu.dev)
     ms, med = gpu.timed_alone(lambda: qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], out),
                               steps, warmup)
@@ -308,6 +311,48 @@ def time_fused_alone(gpu, qb, wl, peaks, peak_src, steps, warmup):
             "frac": round(tflops / peak, 4), "peak": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
             "clusters": info["clusters"], "pairs_per_cluster": info["pairs_per_cluster"],
             "launches": steps, "timing": "alone, launch queued behind a GPU sleep, L2 flushed between launches"}
+
+
+def unfused_torch_forward(torch, wl, d, out):
+    """The same operator as separate PyTorch ops (a per-operator path like the pages'
+    baselines): a cuBLAS bf16 GEMM, RMSNorm and rotate-half RoPE of q and k in fp32,
+    a bf16 cast, and the band scatter as one permuted copy per q/k/v.  A comparator
+    timed beside the fused kernel, not part of the library."""
+    P, B, S, H, D, L = wl.P, wl.B, wl.S, wl.num_heads, 128, wl.H_local
+    T = wl.T
+    y = torch.matmul(d["x"].view(T, wl.hidden), d["w"]).view(T, 3, H, D)
+    qk = y[:, :2].float()
+    rinv = torch.rsqrt(qk.pow(2).mean(-1, keepdim=True) + 1e-6)
+    n = qk * rinv * torch.stack([d["qw"], d["kw"]]).float().view(1, 2, 1, D)
+    cs = d["cs"][d["pos"].view(-1).long()]
+    cos, sin = cs[:, None, None, :64], cs[:, None, None, 64:]
+    n1, n2 = n[..., :64], n[..., 64:]
+    rot = torch.cat([n1 * cos - n2 * sin, n2 * cos + n1 * sin], -1).to(torch.bfloat16)
+    # token (r_s, b, s), head h = r * L + hl -> band r, batch b, global row r_s * S + s, local head hl
+    for g, src in (("q", rot[:, 0]), ("k", rot[:, 1]), ("v", y[:, 2])):
+        out[g].view(P, B, P, S, L, D).copy_(src.reshape(P, B, S, P, L, D).permute(3, 1, 0, 2, 4, 5))
+
+
+def time_unfused_alone(gpu, qb, wl, fused_ms, steps, warmup, inp=None):
+    """The per-operator PyTorch path on `wl`, checked against the fused kernel's
+    output, and the fused kernel's speedup over it."""
+    torch = gpu.torch
+    _, d, plan = fused_setup(gpu, qb, wl, inp)
+    ref = qb.alloc_outputs(plan, wl.B, wl.S, gpu.dev)
+    qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], ref)
+    out = {g: torch.empty_like(t) for g, t in ref.items()}
+    ms, med = gpu.timed_alone(lambda: unfused_torch_forward(torch, wl, d, out), steps, warmup)
+    # the two paths round differently (bf16 GEMM output before the norm here): compare loosely
+    err = max(float((out[g].float() - ref[g].float()).abs().max()) for g in ref)
+    if not err < 0.25:
+        raise RuntimeError(f"per-operator path disagrees with the fused kernel (max |diff| {err})")
+    plan.destroy()
+    return {"ms": round(ms, 5), "ms_median": round(med, 5), "speedup_of_fused": round(ms / fused_ms, 3),
+            "max_abs_diff_vs_fused": round(err, 5),
+            "ops": "torch.matmul (cuBLAS bf16) + fp32 RMSNorm and rotate-half RoPE of q, k + bf16 cast + "
+                   "one permuted copy per q/k/v into the bands",
+            "timing": "alone, launches queued behind a GPU sleep, L2 flushed between repetitions; the speedup "
+                      "divides by the fused kernel alone on the same workload (fused_alone)"}
 
 
 def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra=True):
@@ -595,6 +640,8 @@ def run_gpu(args):
         small = time_fused_alone(gpu, qb, SMALL_FUSED, peaks, peak_src, max(args.steps, 20), args.warmup)
         hc = time_headchunk_alone(gpu, qb, HEADCHUNK, peaks, peak_src, max(args.steps, 20), args.warmup,
                                   rows_extra=False)
+        fused_alone = time_fused_alone(gpu, qb, wl, peaks, peak_src, max(args.steps, 10), args.warmup, inp)
+        unfused = time_unfused_alone(gpu, qb, wl, fused_alone["ms"], max(args.steps, 10), args.warmup, inp)
     clocks.stop()
 
     # ---- rooflines
@@ -640,6 +687,8 @@ def run_gpu(args):
         "pack_schedule": dict(hc["pack_schedule"], workload=HEADCHUNK.name),
         "merge_schedule": dict(hc["merge_schedule"], workload=HEADCHUNK.name),
         "fused_h4096_p4_s4096": small,
+        "fused_alone": fused_alone,
+        "unfused_torch": unfused,
         "step_copies": {"pack_bytes": step_pack_bytes, "merge_bytes": step_merge_bytes,
                         "pack_end_ms": round(statistics.mean(pack_end), 5),
                         "merge_end_ms": round(statistics.mean(merge_end), 5),

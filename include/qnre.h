@@ -30,7 +30,14 @@
  *     caller owns all of it.  No call allocates device memory except
  *     qnre_plan_create (the plan's 16-byte status word).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and returns without waiting for it.
+ *     stream) and returns without waiting for it.  Stream order holds for
+ *     every call.  The layout copies (pack, merge, scatter/gather, sequence
+ *     pack, the composed exchanges) are programmatic dependent launches: their
+ *     blocks may be scheduled while the previous kernel in the stream drains,
+ *     and each waits until that kernel has completed and its writes are
+ *     visible before it reads anything.  Those launched alone (not the
+ *     *_schedule calls) first hint L2 to fetch their source lines, which never
+ *     changes a result.
  *   - Arguments are validated before anything is launched: a call that returns
  *     an error has enqueued nothing and written nothing.
  *   - bf16 values are IEEE bfloat16 bit patterns (the high half of a float32).
