@@ -68,6 +68,21 @@ def test_ragged_multi_tile(layout, rope):
     _full_compare(wl, inp, out)
 
 
+@pytest.mark.parametrize("P,B,S,H,layout", [
+    (1, 1, 96, 2, "bshd"),      # one 256-row tile, three full 32-token warps stored by TMA, the rest past T
+    (2, 3, 32, 4, "fused"),     # every segment one warp long
+    (4, 1, 224, 8, "bshd"),     # 896 tokens: a ragged last pair tile, two-pair clusters
+])
+def test_tma_store_boxes_with_a_ragged_end(P, B, S, H, layout):
+    """S a multiple of 32, so every full warp's 32 tokens lie in one segment and
+    go out as TMA store boxes, while the problem ends inside a row tile."""
+    wl = _wl("tma_tail", P=P, B=B, S=S, H=H, layout=layout)
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    _full_compare(wl, inp, out)
+
+
 def test_odd_head_count_column_tail():
     # 3 heads -> N = 1152 = 4.5 tiles of 256 columns; P = 3 ranks of one head each.
     wl = _wl("oddh", P=3, B=1, S=50, H=3)
