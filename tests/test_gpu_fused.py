@@ -109,6 +109,21 @@ def test_null_positions_use_token_index():
     _full_compare(wl, inp, out, positions=np.arange(wl.T))
 
 
+@pytest.mark.parametrize("layout,rope", [("bshd", "rotate_half"), ("fused", "interleaved")])
+def test_random_positions_into_a_larger_table(layout, rope):
+    """Each token's cos/sin row is positions[token], anywhere in a table longer
+    than the sequence: the rows must follow the given positions, not the token
+    index or the global sequence index."""
+    wl = _wl("randpos", P=2, B=2, S=96, H=4, layout=layout, rope=rope)
+    inp = WL.make_fused_inputs(wl)
+    rng = np.random.default_rng(17)
+    inp.cos_sin = WL.rope_table(5000)
+    inp.positions = rng.integers(0, 5000, size=(wl.P, wl.B, wl.S)).astype(np.int32)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    _full_compare(wl, inp, out)
+
+
 def test_bad_position_gives_nan_rows_and_status():
     wl = _wl("badpos", P=2, B=1, S=64, H=2)
     inp = WL.make_fused_inputs(wl)
