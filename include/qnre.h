@@ -32,7 +32,8 @@
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns without waiting for it.  Stream order holds for
  *     every call.  The layout copies (pack, merge, scatter/gather, sequence
- *     pack, the composed exchanges) are programmatic dependent launches: their
+ *     pack, the composed exchanges) and the three Sage2 kernels are
+ *     programmatic dependent launches: their
  *     blocks may be scheduled while the previous kernel in the stream drains,
  *     and each waits until that kernel has completed and its writes are
  *     visible before it reads anything.  Those launched alone (not the

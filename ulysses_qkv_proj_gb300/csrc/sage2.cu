@@ -9,9 +9,10 @@
 //   1. stats_partial: one CTA per (16 or 32 heads, 256-row chunk of a source
 //      rank, batch); each thread owns 8 channels of one head (16-byte loads,
 //      eight rows in flight) and sums K / takes max|V| down them row by row;
-//   2. stats_final: one warp per (head, batch, 32 channels); thread d adds the chunk sums of
-//      each source rank in order, then the ranks in order -> K mean = sum / U,
-//      V scale = max / 448 and the V reciprocal 448 / max;
+//   2. stats_final: four warps per (head, batch, 32 channels); warp w adds a
+//      quarter of the (source rank, chunk) sums in order, the quarters are added
+//      in warp order -> K mean = sum / U, V scale = max / 448 and the V
+//      reciprocal 448 / max;
 //   3. quantize: one CTA per (head, 64-row global group, batch); each thread
 //      owns 8 channels of 4 (D = 128) or 2 (D = 64) consecutive rows and lands
 //      all of its V, Q and K chunks in shared memory with 16-byte asynchronous
@@ -37,6 +38,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 
 #ifndef QNRE_SAGE2_QUANT_MIN_BLOCKS
 #define QNRE_SAGE2_QUANT_MIN_BLOCKS 4  // resident quantize CTAs per SM the register budget aims at
@@ -125,6 +127,30 @@ __device__ __forceinline__ float reciprocal(float amax, float top) {
   return amax > 0.f ? __fdiv_rn(top, amax) : 0.f;
 }
 
+// The three launches are programmatic dependent launches: each waits here until
+// the grid before it in the stream has completed and its writes are visible,
+// before it reads anything, then lets the next launch begin its set-up.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // 1. Chunk statistics
 // ---------------------------------------------------------------------------
@@ -146,6 +172,7 @@ struct StatsArgs {
 constexpr int kStatsRows = 8;
 template <bool BF16>
 __global__ void __launch_bounds__(256, 2) stats_partial_kernel(const StatsArgs a) {
+  pdl_enter();
   const int tpr = a.D / 8;  // threads per head row
   const int h = blockIdx.x * (256 / tpr) + threadIdx.x / tpr;
   if (h >= a.H) return;
@@ -217,35 +244,54 @@ struct FinalArgs {
 #endif
 };
 
-__global__ void __launch_bounds__(32) stats_final_kernel(const FinalArgs a) {
-  const int d = blockIdx.z * 32 + threadIdx.x, h = blockIdx.x, b = blockIdx.y;
-  float total = 0.f, vm = 0.f;
-  const long long step = static_cast<long long>(a.B) * a.H * a.D;  // between chunks
-  constexpr int kAhead = 16;  // loads in flight per thread; the sum still runs in chunk order
-  for (int r = 0; r < a.P; ++r) {
-    float rank_sum = 0.f;
-    const long long base = ((static_cast<long long>(r) * a.chunks * a.B + b) * a.H + h) * a.D + d;
-    const float* kp = a.ksum + base;
-    const float* vp = a.vmax + base;
-    int c = 0;
-    for (; c + kAhead <= a.chunks; c += kAhead, kp += kAhead * step, vp += kAhead * step) {
-      float ks[kAhead], vs[kAhead];
+// One CTA of four warps per (head, batch, 32 channels): warp w sums its quarter
+// of the (source rank, chunk) partials in order, 16 loads in flight per thread,
+// and the four quarter sums are added in warp order, so the K sum is the same
+// fixed-order fp32 sum on every run.
+constexpr int kFinalWarps = 4;
+__global__ void __launch_bounds__(32 * kFinalWarps) stats_final_kernel(const FinalArgs a) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+  const int d = blockIdx.z * 32 + lane, h = blockIdx.x, b = blockIdx.y;
+  // partial (r, c) sits at ((r * chunks + c) * B + b) * H * D + h * D + d: linear in
+  // i = r * chunks + c with step B * H * D
+  const long long step = static_cast<long long>(a.B) * a.H * a.D;
+  const int n = a.P * a.chunks;
+  const int per = (n + kFinalWarps - 1) / kFinalWarps;
+  const int i0 = min(n, wq * per), i1 = min(n, i0 + per);
+  const long long base = (static_cast<long long>(b) * a.H + h) * a.D + d;
+  const float* kp = a.ksum + base + i0 * step;
+  const float* vp = a.vmax + base + i0 * step;
+  float part = 0.f, vm = 0.f;
+  constexpr int kAhead = 16;  // loads in flight per thread; the sum still runs in order
+  int i = i0;
+  for (; i + kAhead <= i1; i += kAhead, kp += kAhead * step, vp += kAhead * step) {
+    float ks[kAhead], vs[kAhead];
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        ks[u] = kp[u * step];
-        vs[u] = vp[u * step];
-      }
+    for (int u = 0; u < kAhead; ++u) {
+      ks[u] = kp[u * step];
+      vs[u] = vp[u * step];
+    }
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        rank_sum = __fadd_rn(rank_sum, ks[u]);
-        vm = fmaxf(vm, vs[u]);
-      }
+    for (int u = 0; u < kAhead; ++u) {
+      part = __fadd_rn(part, ks[u]);
+      vm = fmaxf(vm, vs[u]);
     }
-    for (; c < a.chunks; ++c, kp += step, vp += step) {
-      rank_sum = __fadd_rn(rank_sum, *kp);
-      vm = fmaxf(vm, *vp);
-    }
-    total = __fadd_rn(total, rank_sum);
+  }
+  for (; i < i1; ++i, kp += step, vp += step) {
+    part = __fadd_rn(part, *kp);
+    vm = fmaxf(vm, *vp);
+  }
+  __shared__ float ps[kFinalWarps][32], pv[kFinalWarps][32];
+  ps[wq][lane] = part;
+  pv[wq][lane] = vm;
+  __syncthreads();
+  if (wq != 0) return;
+  float total = 0.f;
+#pragma unroll
+  for (int w = 0; w < kFinalWarps; ++w) {
+    total = __fadd_rn(total, ps[w][lane]);
+    vm = fmaxf(vm, pv[w][lane]);
   }
   const long long o = (static_cast<long long>(b) * a.H + h) * a.D + d;
   if (QNRE_ACCESS_OK(a.kmean + o, 4, a.ws_ext)) a.kmean[o] = __fdiv_rn(total, static_cast<float>(a.U));
@@ -341,6 +387,7 @@ constexpr int quantize_smem_bytes() {  // V, Q, K landing slots
 // (tensor, u) are contiguous, so they are conflict free.
 template <int RPT, bool BF16>
 __global__ void __launch_bounds__(256, QNRE_SAGE2_QUANT_MIN_BLOCKS) quantize_kernel(const QuantArgs a) {
+  pdl_enter();
   extern __shared__ uint4 land[];  // [3][RPT][256]
   __shared__ float red[8];
   constexpr int kTpr = 4 * RPT;  // threads per row: 16 for D = 128, 8 for D = 64
@@ -650,9 +697,9 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
 #endif
   const int heads_per_cta = 256 / (g.D / 8);
   const dim3 sgrid((g.H + heads_per_cta - 1) / heads_per_cta, g.chunks, P * g.B);
-  if (bf16) stats_partial_kernel<true><<<sgrid, 256, 0, s>>>(sa);
-  else stats_partial_kernel<false><<<sgrid, 256, 0, s>>>(sa);
-  if (cudaGetLastError() != cudaSuccess) return QNRE_ERR_CUDA;
+  if ((bf16 ? launch_pdl(stats_partial_kernel<true>, sgrid, dim3(256), 0, s, sa)
+            : launch_pdl(stats_partial_kernel<false>, sgrid, dim3(256), 0, s, sa)) != cudaSuccess)
+    return QNRE_ERR_CUDA;
 
   FinalArgs fa;
   fa.ksum = sa.ksum;
@@ -671,8 +718,8 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
   fa.ws_ext = Extent{outs[6].lo, outs[6].hi};
   fa.v_scale_ext = Extent{outs[5].lo, outs[5].hi};
 #endif
-  stats_final_kernel<<<dim3(g.H, g.B, g.D / 32), 32, 0, s>>>(fa);
-  if (cudaGetLastError() != cudaSuccess) return QNRE_ERR_CUDA;
+  if (launch_pdl(stats_final_kernel, dim3(g.H, g.B, g.D / 32), dim3(32 * kFinalWarps), 0, s, fa) != cudaSuccess)
+    return QNRE_ERR_CUDA;
 
   QuantArgs qa;
   qa.q = view(q);
@@ -707,11 +754,12 @@ qnre_status_t ulysses_sage2_scatter_qkv(const qnre_tensor4_t* q, const qnre_tens
   qa.k_scale_ext = Extent{outs[4].lo, outs[4].hi};
 #endif
   const dim3 qgrid(g.H, g.S_pad / kKGroup, g.B);
-  if (g.D == 128 && bf16) quantize_kernel<4, true><<<qgrid, 256, quantize_smem_bytes<4>(), s>>>(qa);
-  else if (g.D == 128) quantize_kernel<4, false><<<qgrid, 256, quantize_smem_bytes<4>(), s>>>(qa);
-  else if (bf16) quantize_kernel<2, true><<<qgrid, 256, quantize_smem_bytes<2>(), s>>>(qa);
-  else quantize_kernel<2, false><<<qgrid, 256, quantize_smem_bytes<2>(), s>>>(qa);
-  return from_cuda(cudaGetLastError());
+  cudaError_t e;
+  if (g.D == 128 && bf16) e = launch_pdl(quantize_kernel<4, true>, qgrid, dim3(256), quantize_smem_bytes<4>(), s, qa);
+  else if (g.D == 128) e = launch_pdl(quantize_kernel<4, false>, qgrid, dim3(256), quantize_smem_bytes<4>(), s, qa);
+  else if (bf16) e = launch_pdl(quantize_kernel<2, true>, qgrid, dim3(256), quantize_smem_bytes<2>(), s, qa);
+  else e = launch_pdl(quantize_kernel<2, false>, qgrid, dim3(256), quantize_smem_bytes<2>(), s, qa);
+  return from_cuda(e);
 }
 
 }  // extern "C"
