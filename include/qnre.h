@@ -33,12 +33,11 @@
  *     stream) and returns without waiting for it.  Stream order holds for
  *     every call.  The layout copies (pack, merge, scatter/gather, sequence
  *     pack, the composed exchanges) and the three Sage2 kernels are
- *     programmatic dependent launches: their
- *     blocks may be scheduled while the previous kernel in the stream drains,
- *     and each waits until that kernel has completed and its writes are
- *     visible before it reads anything.  Those launched alone (not the
- *     *_schedule calls) first hint L2 to fetch their source lines, which never
- *     changes a result.
+ *     programmatic dependent launches: their blocks may be scheduled while
+ *     the previous kernel in the stream drains, and each waits until that
+ *     kernel has completed and its writes are visible before it reads
+ *     anything.  Layout copies launched alone (not the *_schedule calls) first
+ *     hint L2 to fetch their source lines, which never changes a result.
  *   - Arguments are validated before anything is launched: a call that returns
  *     an error has enqueued nothing and written nothing.
  *   - bf16 values are IEEE bfloat16 bit patterns (the high half of a float32).
