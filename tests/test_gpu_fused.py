@@ -255,6 +255,40 @@ def test_full_size_sampled_values(name):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("name", ["h7168_p4_s37888_fused", "h8192_p8_b2_s16384"])
+def test_full_size_v_of_every_token(name):
+    """v is the bare projection, so for a random z and every token t,
+    sum_d v[t, h, d] z_d = x_t . (W_vh z) exactly up to v's rounding: this checks
+    the v rows of three heads for every token of the full-size workload (the
+    per-token sample above covers all heads of 640 tokens).  The bound is the
+    per-element bar summed: |sum_d z_d e_d| <= sum_d |z_d| max(2 ulp(v_d), 2e-2)."""
+    wl = WL.FUSED_WORKLOADS[name]
+    inp = WL.make_fused_inputs(wl)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    H, L, D, S, B, P = wl.num_heads, wl.H_local, 128, wl.S, wl.B, wl.P
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal(D)
+    heads = [0, H // 2 + 1, H - 1]
+    w = inp.w
+    U = np.stack([oracle.bf16_to_f64(w[:, (2 * H + h) * D:(2 * H + h + 1) * D]) @ z for h in heads], 1)   # [K, 3]
+    x2 = inp.x.reshape(wl.T, wl.hidden)
+    want = np.concatenate([oracle.bf16_to_f64(x2[i:i + 4096]) @ U for i in range(0, wl.T, 4096)])        # [T, 3]
+    t = np.arange(wl.T)
+    r_s, b, s = t // (B * S), (t // S) % B, t % S
+    zg = torch.from_numpy(z).cuda()
+    for j, h in enumerate(heads):
+        r, hl = h // L, h % L
+        band = out["v"][r, :, :, hl] if wl.layout == "bshd" else out["fused"][r, :, :, hl, 2 * D:]   # [B, S_g, D]
+        vf = band.double()
+        got = (vf @ zg).cpu().numpy()[b, r_s * S + s]                                                   # token order
+        ulp = torch.exp2(torch.floor(torch.log2(vf.abs().clamp_min(2.0 ** -126))) - 7)
+        tol = (zg.abs() * torch.maximum(2 * ulp, torch.full_like(ulp, 2e-2))).sum(-1).cpu().numpy()[b, r_s * S + s]
+        err = np.abs(got - want[:, j])
+        assert np.all(err <= tol), f"{name} head {h}: {np.sum(err > tol)} tokens beyond the bound, worst {err.max():.4g}"
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_exact_placement(name):
     _exact_placement(WL.FUSED_WORKLOADS[name])

@@ -148,6 +148,21 @@ def test_sage2_pages_shape_full_size():
     live = (np.arange(P * L) < U).reshape(P, 1, L, 1, 1, 1)
     buf = np.where(live, buf, np.uint16(0))
     out = _run(buf, P, U, "bf16")
+    # every head, by properties that hold at any size: each group's (Q: 32 rows, K: 64
+    # rows below U) largest code is 127 and each V channel reaches 448 (code 0x7E),
+    # every scale is positive, and codes past U are zero
+    for r in range(P):
+        q, k = out["q"][r].int(), out["k"][r].int()                  # [1, S, H_l, D]
+        assert not q[:, U:].any() and not k[:, U:].any()
+        for codes, grp in ((q, 32), (k, 64)):
+            full = (U // grp) * grp
+            top = codes[:, :full].abs().reshape(1, U // grp, grp, H_l, D).amax(dim=(2, 4))
+            assert bool((top == 127).all()), "a group's largest code is not 127"
+        vcodes = out["v"][r][..., :U].int()                           # [1, D, H_l, U]
+        assert bool(((vcodes & 0x7F).amax(dim=-1) == 0x7E).all()), "a V channel does not reach 448"
+        assert not out["v"][r][..., U:].int().any()
+        for key in ("q_scale", "k_scale", "v_scale"):
+            assert bool((out[key][r] > 0).all()), key
     pick = [0, H_l - 1]                                            # first and last head of each band
     heads = [r * H_l + j for r in range(P) for j in pick]
     ref = _oracle(np.ascontiguousarray(buf[..., heads, :]), U, "bf16")
