@@ -901,7 +901,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=1024,
+    ap.add_argument("--cpu-sample-tokens", type=int, default=8192,
                     help="tokens of the headline workload the CPU-oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-budget-s", type=float, default=90.0,
