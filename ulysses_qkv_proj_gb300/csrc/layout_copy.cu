@@ -128,25 +128,24 @@ __device__ __forceinline__ void copy_block(const Args& a, int seg, int y, int z)
     if constexpr (kPrefetchOnly) {
       if ((u * a.src_unit) % 128 == 0)
         for (long long s = s_begin + lr; s < s_end; s += step) prefetch_l2(sp + s * ss);
-      return;
-    }
-    for (long long s = s_begin + lr; s < s_end; s += step * kUnroll) {
-      U v[kUnroll];
-      bool ok[kUnroll];
+    } else {
+      for (long long s = s_begin + lr; s < s_end; s += step * kUnroll) {
+        U v[kUnroll];
+        bool ok[kUnroll];
 #pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const long long sk = s + k * step;
-        ok[k] = sk < s_end && QNRE_SRC_OK(sp + sk * ss);
-        if (ok[k]) v[k] = ld_row<U, kStream>(sp + sk * ss);
-      }
+        for (int k = 0; k < kUnroll; ++k) {
+          const long long sk = s + k * step;
+          ok[k] = sk < s_end && QNRE_SRC_OK(sp + sk * ss);
+          if (ok[k]) v[k] = ld_row<U, kStream>(sp + sk * ss);
+        }
 #pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const long long sk = s + k * step;
-        if (ok[k] && QNRE_DST_OK(dp + sk * ds)) st_row<U, kStream>(dp + sk * ds, v[k]);
+        for (int k = 0; k < kUnroll; ++k) {
+          const long long sk = s + k * step;
+          if (ok[k] && QNRE_DST_OK(dp + sk * ds)) st_row<U, kStream>(dp + sk * ds, v[k]);
+        }
       }
     }
-  } else {
-    if constexpr (kPrefetchOnly) return;
+  } else if constexpr (!kPrefetchOnly) {
     const long long n = (s_end - s_begin) * a.units;
     for (long long e = threadIdx.x; e < n; e += kThreads) {
       const long long s = s_begin + e / a.units;
