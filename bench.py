@@ -355,10 +355,11 @@ def time_unfused_alone(gpu, qb, wl, fused_ms, steps, warmup, inp=None):
                       "divides by the fused kernel alone on the same workload (fused_alone)"}
 
 
-def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra=True):
+def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup):
     """Pack and merge over the pages' head-chunk shape: every chunk of the schedule
     for every virtual rank, per chunk (one launch each) and as schedule calls (one
-    launch per rank); optionally the ordinary / composed exchanges and Sage2."""
+    launch per rank); then the ordinary and composed exchanges and Sage2 over the
+    same q/k/v."""
     torch = gpu.torch
     buf = gpu.bf16(WL.make_headchunk_buffer(wl.B, wl.S_global, wl.num_heads, wl.D))
     W, L, D, S, P = wl.P, wl.H_local, wl.D, wl.S, wl.P
@@ -426,8 +427,6 @@ def time_headchunk_alone(gpu, qb, wl, peaks, peak_src, steps, warmup, rows_extra
     for r in range(P):
         if not torch.equal(merged[r], views[r][0]):
             raise RuntimeError("schedule pack -> merge did not reproduce q")
-    if not rows_extra:
-        return res
 
     # ordinary and composed exchanges over the same P virtual ranks
     ranks = buf.view(P, S, 3, wl.num_heads, D)                 # [P*B, S, 3, H, D] with B = 1
@@ -638,8 +637,7 @@ def run_gpu(args):
     # ---- rows timed alone
     with clocks.section("alone"):
         small = time_fused_alone(gpu, qb, SMALL_FUSED, peaks, peak_src, max(args.steps, 20), args.warmup)
-        hc = time_headchunk_alone(gpu, qb, HEADCHUNK, peaks, peak_src, max(args.steps, 20), args.warmup,
-                                  rows_extra=False)
+        hc = time_headchunk_alone(gpu, qb, HEADCHUNK, peaks, peak_src, max(args.steps, 20), args.warmup)
         fused_alone = time_fused_alone(gpu, qb, wl, peaks, peak_src, max(args.steps, 10), args.warmup, inp)
         unfused = time_unfused_alone(gpu, qb, wl, fused_alone["ms"], max(args.steps, 10), args.warmup, inp)
     clocks.stop()
@@ -686,6 +684,11 @@ def run_gpu(args):
         "merge": dict(hc["merge_per_chunk"], workload=HEADCHUNK.name),
         "pack_schedule": dict(hc["pack_schedule"], workload=HEADCHUNK.name),
         "merge_schedule": dict(hc["merge_schedule"], workload=HEADCHUNK.name),
+        "pack_output_sequence_chunk": dict(hc["pack_output_sequence_chunk"], workload=HEADCHUNK.name),
+        "layout_rows": {k: dict(hc[k], workload=HEADCHUNK.name)
+                        for k in ("scatter_heads", "gather_heads", "scatter_qkv_head_chunk",
+                                  "gather_output_head_chunk")},
+        "sage2": dict(hc["sage2_scatter_qkv"], workload=HEADCHUNK.name),
         "fused_h4096_p4_s4096": small,
         "fused_alone": fused_alone,
         "unfused_torch": unfused,
@@ -878,7 +881,7 @@ def run_gpu_workload(args):
     elif name in WL.HEADCHUNK_WORKLOADS:
         wl = WL.HEADCHUNK_WORKLOADS[name]
         with clocks.section("alone"):
-            res = time_headchunk_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup, rows_extra=True)
+            res = time_headchunk_alone(gpu, qb, wl, peaks, peak_src, args.steps, args.warmup)
         p = res["pack_per_chunk"]
         line = {"metric": "head-chunk pack/merge GB/s", "value": p["GB/s"], "unit": "GB/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": p["ms"], "higher_is_better": True,
