@@ -299,7 +299,7 @@ def test_sage2_pins_catch_planted_mistake(name, mutant, monkeypatch, golden_dir)
     tripped = []
     for check in CHECKS:
         try:
-            with np.errstate(all="ignore"):   # a mutant may make NaNs; only the verdict matters
+            with np.errstate(all="ignore"):   # a mutant may make NaNs; only the outcome matters
                 check()
         except (AssertionError, ValueError, IndexError):
             tripped.append(check.__name__)
