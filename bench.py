@@ -661,15 +661,10 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/hidden) weights, 1+0.1N(0,1) norm weights)",
-        "config": {"workload": f"{wl.name}: P={wl.P} B={wl.B} S_local={wl.S} S_global={wl.S_global} "
-                               f"hidden={wl.hidden} heads={wl.num_heads} layout={wl.layout} rope={wl.rope_style}; "
-                               f"pack/merge schedule {[list(b) for b in SCHEDULE]} over H_local={L}",
-                   "tokens_per_step": wl.T, "P": wl.P, "B": wl.B, "S_local": wl.S, "hidden": wl.hidden,
-                   "num_heads": wl.num_heads, "layout": wl.layout, "schedule": [list(b) for b in SCHEDULE],
-                   "l2": "inputs (2.1 GB) larger than L2, and L2 flushed (512 MB write) between steps",
-                   "streams": "one" if args.no_overlap else "fused on the main stream, pack/merge on a second",
-                   "reserved_sms": reserved, "fused_clusters": info["clusters"],
-                   "pairs_per_cluster": info["pairs_per_cluster"], "parallelism": "one GPU"},
+        "config": headline_config(),
+        "execution": {"streams": "one" if args.no_overlap else "fused on the main stream, pack/merge on a second",
+                      "reserved_sms": reserved, "fused_clusters": info["clusters"],
+                      "pairs_per_cluster": info["pairs_per_cluster"], "parallelism": "one GPU"},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": sustained, "unit": "TFLOP/s",
                      "frac": round(tflops / sustained, 4), "traffic": profiled_traffic(wl.name),
                      "kernel": "fused_qkv_kernel", "flops_per_launch": flops,
@@ -795,6 +790,18 @@ def cpu_baseline(n_tokens: int):
             "extrapolated": True, "seconds": round(dt, 3)}
 
 
+def headline_config():
+    """The headline workload, as both arms report it."""
+    wl = WORKLOAD
+    sched = [list(b) for b in SCHEDULE]
+    return {"workload": f"{wl.name}: P={wl.P} B={wl.B} S_local={wl.S} S_global={wl.S_global} "
+                        f"hidden={wl.hidden} heads={wl.num_heads} layout={wl.layout} rope={wl.rope_style}; "
+                        f"pack/merge schedule {sched} over H_local={wl.H_local}",
+            "tokens_per_step": wl.T, "P": wl.P, "B": wl.B, "S_local": wl.S, "hidden": wl.hidden,
+            "num_heads": wl.num_heads, "layout": wl.layout, "schedule": sched,
+            "l2": "inputs (2.1 GB) larger than L2, and L2 flushed (512 MB write) between steps"}
+
+
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
@@ -820,8 +827,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "tokens_per_step_sample": tok,
-                                        "parallelism": "host cores"},
+        "data": "synthetic", "config": headline_config(),
+        "execution": {"parallelism": "host cores", "tokens_per_step_sample": tok},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

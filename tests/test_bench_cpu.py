@@ -68,7 +68,9 @@ def test_reference_arm_line_rank0():
     assert r.returncode == 0, r.stderr[-800:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
-    assert line["config"]["workload"] == bench.WORKLOAD.name
+    # the same config object as the GPU arm's line, so the two lines compare like for like
+    assert line["config"] == bench.headline_config()
+    assert line["config"]["workload"].startswith(bench.WORKLOAD.name + ":")
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
 
 
