@@ -62,8 +62,9 @@ HEADCHUNK = WL.HEADCHUNK_WORKLOADS[WL.BENCH_HEADCHUNK]
 SCHEDULE = WL.BENCH_SCHEDULE
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# the fused kernel and the host code that sets its launch shape and raster
 FUSED_SOURCES = ["ulysses_qkv_proj_gb300/csrc/fused_qkv.cu", "ulysses_qkv_proj_gb300/csrc/fused_qkv.cuh",
-                 "ulysses_qkv_proj_gb300/csrc/ptx.cuh"]
+                 "ulysses_qkv_proj_gb300/csrc/ptx.cuh", "ulysses_qkv_proj_gb300/csrc/qnre_api.cu"]
 TRAFFIC_FILE = "profiles/traffic.json"
 
 

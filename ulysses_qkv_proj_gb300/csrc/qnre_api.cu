@@ -13,7 +13,7 @@
 #include <algorithm>
 
 #ifndef QNRE_RASTER_L2_MB
-#define QNRE_RASTER_L2_MB 48  // L2 share for the resident x panels of a row-tile group
+#define QNRE_RASTER_L2_MB 32  // L2 share for the resident x panels of a row-tile group
 #endif
 #include <cstdint>
 #include <mutex>
@@ -377,7 +377,9 @@ qnre_status_t forward_impl(qnre_plan_t plan, int B, int S_local, const void* x, 
   a.num_tiles = a.num_m_tiles * a.num_n_tiles;
   // Raster: groups of group_m row tiles sweep every column tile, rows fastest.
   // The group's x panels (256 rows x hidden each) stay resident in L2 while W
-  // streams past; keep them to about 48 MB of the 129 MB L2.
+  // streams past; keep them to about 32 MB of the 129 MB L2 (a budget of 28-32
+  // MB ran the 32768-token, hidden-8192 projection fastest both alone and under
+  // the power cap; 16, 40 and 48 MB were slower).
   const int64_t panel_bytes = static_cast<int64_t>(qnre::kPairM) * K * 2;
   a.group_m = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(m_tiles, (static_cast<int64_t>(QNRE_RASTER_L2_MB) << 20) / panel_bytes)));
