@@ -631,6 +631,30 @@ def run_gpu(args):
     if not torch.equal(host_out[0]["q"], out["q"].cpu()):
         raise RuntimeError("end-to-end projection differs from the device-resident one")
     e2e_value = wl.T / (e2e_ms * 1e-3)
+
+    # the host link alone on this machine: the same copies as one step, no compute
+    def copies_only():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(main)
+        h2d_s.wait_event(e0)
+        d2h_s.wait_event(e0)
+        xin, qin = dev_in[0]
+        with torch.cuda.stream(h2d_s):
+            xin.copy_(x_host, non_blocking=True)
+            qin.copy_(qkv_host, non_blocking=True)
+        ho, hm = host_out
+        with torch.cuda.stream(d2h_s):
+            for g, t in sets[1]["out"].items():
+                ho[g].copy_(t, non_blocking=True)
+            hm.copy_(sets[1]["merged"], non_blocking=True)
+        main.wait_stream(h2d_s)
+        main.wait_stream(d2h_s)
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    link_ms = min(copies_only() for _ in range(3))
     plan.destroy()
     del sets, dev_in, host_out, packed, merged, qkv, out, d
     torch.cuda.empty_cache()
@@ -696,7 +720,9 @@ def run_gpu(args):
                                 if not args.no_overlap else "end times from the step's start, one stream"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "pipelined: step i's D2H and step i+1's H2D overlap compute"},
+                "link_ms_per_step": round(link_ms, 4), "frac_of_link": round(link_ms / e2e_ms, 4),
+                "note": "pipelined: step i's D2H and step i+1's H2D overlap compute; link_ms_per_step is the "
+                        "same copies alone (both directions at once, no compute), the floor on this box"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": step_clk,
         "clocks_sections": {k: clocks.summary(k) for k in ("warm_l2", "e2e", "alone")},
