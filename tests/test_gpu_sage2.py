@@ -167,3 +167,18 @@ def test_sage2_pages_shape_full_size():
     heads = [r * H_l + j for r in range(P) for j in pick]
     ref = _oracle(np.ascontiguousarray(buf[..., heads, :]), U, "bf16")
     _assert_equal(out, ref, P, heads=pick)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_sage2_random_shapes(seed):
+    """Seeded random (P, B, L, H, D, used prefix, dtype) against the oracle."""
+    rng = np.random.default_rng(700 + seed)
+    P = int(rng.choice([1, 2, 3, 4, 8]))
+    B = int(rng.integers(1, 3))
+    L = int(rng.integers(1, 400))
+    H = P * int(rng.integers(1, 4))
+    D = int(rng.choice([64, 128]))
+    U = int(rng.integers(1, P * L + 1))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    buf = _case(P, B, L, H, D, U, dtype, seed=seed)
+    _assert_equal(_run(buf, P, U, dtype), _oracle(buf, U, dtype), P)
