@@ -88,9 +88,15 @@ def test_head_chunk_pack_merge(seed):
         qb.ulysses_merge_output_head_chunk(o[..., 2 * D:], W, L, off, m1)
         ref = oracle.merge_output_head_chunk(w[..., 2 * D:], W, L, off, ref)
     qb.ulysses_merge_output_head_chunk_schedule([o[..., 2 * D:] for o in outs], W, L, [off for off, _ in sched], m2)
+    # the same merges from contiguous received bands (heads back to back)
+    m3, m4 = _dev(fill), _dev(fill)
+    recv = [o[..., 2 * D:].contiguous() for o in outs]
+    for (off, _), r in zip(sched, recv):
+        qb.ulysses_merge_output_head_chunk(r, W, L, off, m3)
+    qb.ulysses_merge_output_head_chunk_schedule(recv, W, L, [off for off, _ in sched], m4)
     torch.cuda.synchronize()
-    assert np.array_equal(_host(m1), ref)
-    assert np.array_equal(_host(m2), ref)
+    for m in (m1, m2, m3, m4):
+        assert np.array_equal(_host(m), ref)
 
 
 @pytest.mark.parametrize("seed", range(N_CASES))
