@@ -572,11 +572,14 @@ def run_gpu(args):
             "note": "no L2 flush between steps (the step's 2.1 GB of inputs exceed L2 anyway)"}
 
     # ---- end to end: every step copies its inputs from pinned host memory and its
-    # results back.  Two device buffer sets and separate copy streams let step i's
-    # device->host copy and step i+1's host->device copy overlap the compute.
-    sets = [primary, {"out": {g: torch.empty_like(t) for g, t in out.items()},
-                      "packed": [torch.empty_like(t) for t in packed], "merged": torch.empty_like(merged)}]
-    dev_in = [(torch.empty_like(d["x"]), torch.empty_like(qkv)) for _ in range(2)]
+    # results back.  Three device buffer sets and separate copy streams let step
+    # i's device->host copy and the next steps' host->device copies overlap the
+    # compute, with a step of slack either way.
+    n_sets = 3
+    sets = [primary] + [{"out": {g: torch.empty_like(t) for g, t in out.items()},
+                         "packed": [torch.empty_like(t) for t in packed], "merged": torch.empty_like(merged)}
+                        for _ in range(n_sets - 1)]
+    dev_in = [(torch.empty_like(d["x"]), torch.empty_like(qkv)) for _ in range(n_sets)]
     host_out = ({g: torch.empty_like(t, device="cpu").pin_memory() for g, t in out.items()},
                 torch.empty_like(merged, device="cpu").pin_memory())
     h2d = x_host.numel() * 2 + qkv_host.numel() * 2
@@ -594,17 +597,17 @@ def run_gpu(args):
         e_start.record(main)
         h2d_s.wait_event(e_start)
         for i in range(n):
-            b = i % 2
+            b = i % n_sets
             xin, qin = dev_in[b]
-            if i >= 2:
-                h2d_s.wait_event(ev_comp[i - 2])   # step i-2 has finished reading this input set
+            if i >= n_sets:
+                h2d_s.wait_event(ev_comp[i - n_sets])   # the step before has finished reading this input set
             with torch.cuda.stream(h2d_s):
                 xin.copy_(x_host, non_blocking=True)
                 qin.copy_(qkv_host, non_blocking=True)
             ev_in[i].record(h2d_s)
             main.wait_event(ev_in[i])
-            if i >= 2:
-                main.wait_event(ev_out[i - 2])     # this output set has been copied out
+            if i >= n_sets:
+                main.wait_event(ev_out[i - n_sets])     # this output set has been copied out
             step(xin, qin, bufs=sets[b])
             ev_comp[i].record(main)
             d2h_s.wait_event(ev_comp[i])
@@ -621,7 +624,7 @@ def run_gpu(args):
 
     # the first copy from or into a freshly pinned buffer pays its mapping (tens
     # of ms): warm-up passes touch every buffer before the timed one
-    e2e_pass(max(2, args.warmup))
+    e2e_pass(max(n_sets, args.warmup))
     n = args.steps
     with clocks.section("e2e"):
         e2e_total = e2e_pass(n)
