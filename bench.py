@@ -22,10 +22,17 @@ launches, L2 flushed between repetitions):
   * "pack" / "merge": the head-chunk pack and merge of [1, 37760, 56, 128] over
     two virtual ranks with the schedule [7, 14, 7] (the pages' shape), per
     chunk and as schedule calls;
+  * "pack_output_sequence_chunk", "layout_rows" (scatter/gather heads and the
+    composed head-chunk exchanges) and "sage2" over the same q/k/v;
   * "fused_h4096_p4_s4096": the fused op alone on the 4096-token workload;
   * "fused_alone" and "unfused_torch": the headline workload's fused op alone,
     and the same operator as separate PyTorch ops (cuBLAS GEMM, RMSNorm, RoPE,
     band scatter) with the fused kernel's speedup over it.
+
+"e2e" runs the step through the same API with every step's inputs copied
+from pinned host memory and its outputs copied back (three buffer sets, copy
+streams overlapping compute), beside the same copies timed alone (the host
+link's floor on the box).
 
 This benchmark runs on one GPU: it refuses WORLD_SIZE > 1 and --gpus > 1 (the
 fused kernel's two-pair clusters multicast W inside a cluster, and nothing on
