@@ -4,6 +4,8 @@ Values: |gpu - oracle| <= max(2 bf16 ulp(oracle), 2e-2) per element.
 Placement: bit-exact, checked with integer-coded inputs (QNRE_FLAG_EPILOGUE_OFF)
 whose projection is exact in every precision.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -286,6 +288,27 @@ def test_full_size_v_of_every_token(name):
         tol = (zg.abs() * torch.maximum(2 * ulp, torch.full_like(ulp, 2e-2))).sum(-1).cpu().numpy()[b, r_s * S + s]
         err = np.abs(got - want[:, j])
         assert np.all(err <= tol), f"{name} head {h}: {np.sum(err > tol)} tokens beyond the bound, worst {err.max():.4g}"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["h7168_p4_s37888_fused", "h8192_p8_b2_s16384"])
+def test_full_size_qk_norms_of_every_token(name):
+    """With unit norm weights RMSNorm leaves every q and k head row with mean square 1
+    (less eps / (ms + eps)) and RoPE turns each pair without changing its norm, so
+    every q and k row of every token has sum of squares 128 up to the bf16 rounding
+    of its elements (at most 2^-8 relative each, so 2^-7 relative on each square
+    and on the sum: |S - 128| <= 1, with 0.01 for eps and the fp32 arithmetic)."""
+    wl = WL.FUSED_WORKLOADS[name]
+    inp = WL.make_fused_inputs(wl)
+    one = np.full(128, 0x3F80, np.uint16)                    # bf16 1.0
+    inp = dataclasses.replace(inp, q_norm_w=one, k_norm_w=one)
+    _, out, status = _run(wl, _dev_inputs(inp))
+    assert status == 0
+    for gi, g in enumerate("qk"):
+        t = out[g] if wl.layout == "bshd" else out["fused"][..., gi * 128:(gi + 1) * 128]
+        dev = (t.double().square().sum(-1) - 128.0).abs()    # [P, B, S_global, H_local]
+        worst = dev.max().item()
+        assert worst <= 1.01, f"{name}/{g}: {int((dev > 1.01).sum())} rows beyond the bound, worst {worst:.4g}"
 
 
 @pytest.mark.slow
