@@ -113,3 +113,37 @@ def test_noalloc_rejects_before_enqueueing():
     assert fn(512, 4, 2, 0, 0, 0, 1 << 20, 1 << 12, *args) == 5  # tokens beyond the kernel's range
     torch.cuda.synchronize()
     assert status.item() == 12345                                # nothing was enqueued
+
+
+def test_noalloc_forward_replays_in_a_cuda_graph():
+    """After its first call on the device, the call can be captured: a CUDA graph of
+    one no-alloc forward, replayed on fresh inputs copied into the captured buffers,
+    gives the same bits as a one-pair plan forward on those inputs each time."""
+    fn = _noalloc()
+    wl = WL.FusedWorkload("noalloc_g", P=2, B=1, S=160, num_heads=4)
+    inp = _host_inputs(wl)
+    d = _inputs(wl, inp=inp)
+    plan = qb.Plan(wl.hidden, wl.num_heads, wl.P, wl.layout, max_tokens=wl.B * wl.S, flags=qb.FLAG_ONE_PAIR)
+    out = qb.alloc_outputs(plan, wl.B, wl.S)
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    assert _call_noalloc(fn, wl, d, out, status) == 0           # set-up call, outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        assert _call_noalloc(fn, wl, d, out, status) == 0
+    rng = np.random.default_rng(3)
+    for rep in range(2):
+        x_new = rng.standard_normal(inp.x.shape).astype(np.float32)
+        d["x"].copy_(to_dev_bf16(WL.f32_to_bf16_bits(x_new)))
+        for t in out.values():
+            t.view(torch.int16).fill_(-1)
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = qb.alloc_outputs(plan, wl.B, wl.S)
+        qb.qnre_forward(plan, d["x"], d["w"], d["qw"], d["kw"], d["cs"], d["pos"], ref)
+        torch.cuda.synchronize()
+        assert status.item() == 0 and plan.device_status() == 0
+        for g in ref:
+            assert np.array_equal(to_host_bits(out[g]), to_host_bits(ref[g])), f"replay {rep}/{g}"
